@@ -1,0 +1,477 @@
+#!/usr/bin/env python3
+"""float_vif throughput on GB300: frame pairs per second (4 scales).
+
+A step is one pass of the whole path (taps, decimation to scales 1..3, the
+statistic and terms at every scale, row sums, per-scale sums and scores) over
+one batch of the workload's frames, through libfvif's C ABI.
+
+  value  device-resident inputs (uploaded before the timed region),
+         fvif_score_async on one stream, CUDA events around K steps.
+  e2e    page-locked host inputs through fvif_score_host: the host->device
+         copies of every step's frames and the device->host read of the
+         scores are inside the timed region.
+  roofline  the dominant kernel (the scale-0 statistic launch), timed by the
+         library's own events around each launch on the launching stream.
+  cpu_baseline  the CPU oracle (test infrastructure, never tuned) on a
+         bounded sample of the same workload, frame-parallel on host cores.
+
+``--impl reference`` times the oracle alone as the reference arm.
+Multi-GPU (torchrun): every rank scores its own batch (weak scaling, no
+data-path collective); the step time is the maximum over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from vmaf_float_vif_gb300 import synthetic as S  # noqa: E402
+
+PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC_PATH = os.path.join(ROOT, "profiles", "stats_scale0_traffic.json")
+KERNEL_SOURCES = ["fvif_kernels.cuh", "fvif_dispatch.cuh", "fvif_stats_u8.cu",
+                  "fvif_stats_u16.cu", "fvif_internal.h"]
+SMS = 152
+FP32_LANES_PER_SM = 128
+FALLBACK_HBM_GBS = 6800.0
+
+WORKLOADS = {
+    # name: (case, frames per step, kernelscale)
+    "c5_4k_10b": ("c5_4k_10b", 240, 1.0),
+    "c5_4k_10b_ks0.5": ("c5_4k_10b", 240, 0.5),
+    "c5_4k_10b_ks2": ("c5_4k_10b", 240, 2.0),
+    "c4_4k_8b": ("c4_4k_8b", 20, 1.0),
+    "c2_1080p_10b": ("c2_checker_1px_10b", 240, 1.0),
+    "c3_1080p_16b": ("c3_bright_1080p_16b", 240, 1.0),
+}
+
+
+def describe(name, frames_override=None):
+    case_name, frames, ks = WORKLOADS[name]
+    frames = frames_override or frames
+    c = S.CASES[case_name]
+    return ("%s: %dx%d %d-bit luma pairs, %d frames per step in chunks of 16, "
+            "kernelscale %g, sigma_nsq %g" % (case_name, c.w, c.h, c.bitdepth,
+                                              frames, ks, c.nsq))
+
+
+def make_inputs(name, frames_override=None):
+    case_name, frames, _ = WORKLOADS[name]
+    frames = frames_override or frames
+    case = S.CASES[case_name]
+    if case.frames >= frames:
+        return case, case.batch(range(frames))
+    return case, S.streamed_batch(case, frames)
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")),
+            int(os.environ.get("LOCAL_RANK", "0")),
+            int(os.environ.get("WORLD_SIZE", "1")))
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,"
+              "clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu),
+                 "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [],
+                    "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing
+
+
+def oracle_rate(case, ref, dist, ks, frames_wanted, threads):
+    import oracle
+    oracle.build()
+    oracle.lib()
+    n = min(frames_wanted, ref.shape[0])
+    t0 = time.perf_counter()
+    oracle.score(ref[:n], dist[:n], case.bitdepth, ks, case.nsq,
+                 threads=threads)
+    dt = time.perf_counter() - t0
+    return n / dt, n, dt
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# ---------------------------------------------------------------------------
+
+
+def kernel_hash():
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "vmaf_float_vif_gb300", "csrc", f),
+                  "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def load_traffic(workload):
+    """Per-launch DRAM bytes of the scale-0 statistic kernel from a committed
+    ncu summary, only if it was taken on the current kernel sources."""
+    try:
+        with open(TRAFFIC_PATH) as f:
+            t = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if t.get("kernel_hash") != kernel_hash():
+        return None
+    return t.get("per_launch_bytes", {}).get(workload)
+
+
+def stats_ops_per_pixel(ntaps: int) -> int:
+    """Algorithmic fp32 operations of the statistic per pixel: five
+    quantities, two passes, ntaps products and ntaps-1 sums each, plus the
+    three products x*x, y*y, x*y."""
+    return 10 * (2 * ntaps - 1) + 3
+
+
+def run_ours(args):
+    import torch
+    import vmaf_float_vif_gb300 as fv
+
+    rank, local_rank, world = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local_rank)
+    fv.build()
+
+    case, (ref, dist_np) = make_inputs(args.workload, args.frames)
+    _, frames, ks = WORKLOADS[args.workload]
+    frames = args.frames or frames
+    bpp = case.bytes_per_pair
+
+    def as_dev(a):
+        if a.dtype == np.uint16:
+            a = a.view(np.int16)
+        return torch.from_numpy(a).to("cuda")
+
+    r_dev, d_dev = as_dev(ref), as_dev(dist_np)
+    out = torch.empty(4 * frames, dtype=torch.float64, device="cuda")
+    stream = torch.cuda.Stream()
+    ctx = fv.Context(case.w, case.h, case.bitdepth, ks, case.nsq)
+    ctx.set_stream(stream)
+    n0 = len(ctx.taps(0))
+    chunk = ctx.chunk_frames
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            ctx.score_async(r_dev, d_dev, out)
+    torch.cuda.synchronize()
+
+    ctx.profile(True)
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clocks:
+        start.record(stream)
+        for _ in range(args.steps):
+            ctx.score_async(r_dev, d_dev, out)
+        stop.record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    ms_total = start.elapsed_time(stop)
+    prof = ctx.profile_read()
+    ctx.profile(False)
+    scores = out.cpu().numpy().reshape(-1, 4)
+    if not np.all(np.isfinite(scores)):
+        raise RuntimeError("non-finite scores")
+
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms_total], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / args.steps
+    value = frames * args.steps * world / (ms_total / 1e3)
+
+    # e2e: host buffers, copies inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        pr = torch.from_numpy(ref.view(np.int16) if ref.dtype == np.uint16
+                              else ref).pin_memory()
+        pd = torch.from_numpy(dist_np.view(np.int16)
+                              if dist_np.dtype == np.uint16
+                              else dist_np).pin_memory()
+        hr = pr.numpy().view(ref.dtype)
+        hd = pd.numpy().view(dist_np.dtype)
+        ctx.set_stream(None)
+        for _ in range(max(1, args.warmup)):
+            ctx.score_host(hr, hd)
+        barrier()
+        torch.cuda.synchronize()
+        e_start = torch.cuda.Event(enable_timing=True)
+        e_stop = torch.cuda.Event(enable_timing=True)
+        t0 = time.perf_counter()
+        e_start.record()
+        for _ in range(args.e2e_steps):
+            host_scores = ctx.score_host(hr, hd)
+        e_stop.record()
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+        barrier()
+        if world > 1:
+            import torch.distributed as dist
+            t = torch.tensor([wall], dtype=torch.float64, device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            wall = float(t.item())
+        if not np.array_equal(host_scores, scores):
+            raise RuntimeError("fvif_score_host and fvif_score_async differ")
+        e2e = {"value": frames * args.e2e_steps * world / wall,
+               "unit": "frame-pairs/s",
+               "h2d_bytes_per_step": int(ref.nbytes + dist_np.nbytes),
+               "d2h_bytes_per_step": int(scores.nbytes),
+               "ms_per_step": 1e3 * wall / args.e2e_steps,
+               "api": "fvif_score_host (page-locked host inputs)"}
+
+    if rank != 0:
+        ctx.close()
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+
+    peaks = {}
+    try:
+        with open(PEAKS_PATH) as f:
+            peaks = json.load(f)
+    except (OSError, ValueError):
+        pass
+    hbm_peak = peaks.get("hbm_gbs")
+    hbm_src = "of measured" if hbm_peak else "of fallback"
+    hbm_peak = hbm_peak or FALLBACK_HBM_GBS
+    clk = clocks.summary()
+    sm_max = clk.get("sm_max_mhz") or peaks.get("sm_max_mhz") or 2070.0
+
+    st0_ms, st0_n = prof["stats_scale0"]
+    launches_total = sum(n for _, n in prof.values())
+    px0 = case.w * case.h
+    ops_launch = chunk * px0 * stats_ops_per_pixel(n0)
+    avg_ms = st0_ms / max(1, st0_n)
+    achieved = ops_launch / (avg_ms / 1e3) / 1e12
+    alu_peak = SMS * FP32_LANES_PER_SM * sm_max * 1e6 / 1e12
+    traffic = load_traffic(args.workload)
+    kernel_shares = {k: {"ms": v[0], "launches": v[1],
+                         "share": v[0] / max(1e-9, sum(x[0] for x in
+                                                       prof.values()))}
+                     for k, v in prof.items()}
+
+    line = {
+        "metric": "float_vif frame-pairs/s, 4 scales (%dx%d %d-bit)" %
+                  (case.w, case.h, case.bitdepth),
+        "value": value,
+        "unit": "frame-pairs/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {
+            "workload": describe(args.workload, args.frames),
+            "frames_per_step": frames,
+            "chunk_frames": chunk,
+            "taps": [len(ctx.taps(s)) for s in range(4)],
+            "l2": "no flush: inputs %.2f GB per step exceed the 129 MB L2" %
+                  (frames * bpp / 1e9),
+            "hbm_fraction_algorithmic": value / world * bpp / 1e9 / hbm_peak,
+            "hbm_fraction_note": "input bytes only (%d B per pair) against "
+                                 "%.1f GB/s %s" % (bpp, hbm_peak, hbm_src),
+            "kernels": kernel_shares,
+        },
+        "roofline": {
+            "kernel": "stats_kernel, scale 0 (%d taps), %d frames per launch"
+                      % (n0, chunk),
+            "bound": "alu",
+            "achieved": achieved,
+            "peak": alu_peak,
+            "unit": "TFLOP/s",
+            "frac": achieved / alu_peak,
+            "traffic": traffic,
+            "per_unit": "%d fp32 ops per pixel" % stats_ops_per_pixel(n0),
+            "launch_ms": avg_ms,
+            "peak_note": "%d SMs x %d fp32 lanes x %.0f MHz, one non-fused op "
+                         "per lane per clock" % (SMS, FP32_LANES_PER_SM,
+                                                 sm_max),
+        },
+        "gpu_launches": int(launches_total),
+        "clocks": clk,
+    }
+    ctx.close()
+    if e2e:
+        line["e2e"] = e2e
+    if not args.no_cpu_baseline:
+        cores = host_cores()
+        rate, n, dt = oracle_rate(case, ref, dist_np, ks, cores, cores)
+        line["cpu_baseline"] = {
+            "value": rate, "unit": "frame-pairs/s", "cores": cores,
+            "kind": "oracle",
+            "sample": "%d frames of the workload, one per host thread, "
+                      "%.1f s wall" % (n, dt)}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_reference(args):
+    rank, _, world = dist_env()
+    if rank != 0:
+        return
+    case, (ref, dist_np) = make_inputs_sample(args.workload)
+    _, frames, ks = WORKLOADS[args.workload]
+    cores = host_cores()
+    per_step = min(cores, ref.shape[0])
+    for _ in range(args.warmup):
+        oracle_rate(case, ref, dist_np, ks, per_step, cores)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_rate(case, ref, dist_np, ks, per_step, cores)
+    wall = time.perf_counter() - t0
+    value = per_step * args.steps / wall
+    line = {
+        "impl": "reference",
+        "metric": "float_vif frame-pairs/s, 4 scales (%dx%d %d-bit)" %
+                  (case.w, case.h, case.bitdepth),
+        "value": value,
+        "unit": "frame-pairs/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": 1e3 * wall / args.steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": describe(args.workload),
+                   "frames_per_step": per_step,
+                   "note": "each step scores a bounded sample of the "
+                           "workload (one frame per host thread)"},
+        "cpu_baseline": {"value": value, "unit": "frame-pairs/s",
+                         "cores": cores, "kind": "oracle",
+                         "sample": "%d frames per step" % per_step},
+        "e2e": {"value": value, "unit": "frame-pairs/s",
+                "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def make_inputs_sample(name):
+    case_name, frames, _ = WORKLOADS[name]
+    case = S.CASES[case_name]
+    n = min(frames, max(1, host_cores()), 16)
+    if case.frames >= n:
+        return case, case.batch(range(n))
+    return case, S.streamed_batch(case, n)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="c5_4k_10b")
+    ap.add_argument("--frames", type=int, default=None,
+                    help="frames per step (default: the workload's)")
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        print("note: fewer than 3 warm-up steps", file=sys.stderr)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

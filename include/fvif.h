@@ -1,0 +1,145 @@
+/*
+ * fvif.h -- C ABI of libfvif, the 4-scale float VIF score on one GB300
+ * (sm_103a) GPU.
+ *
+ * The score is the float_vif feature of a VMAF fork as its documentation
+ * describes it:
+ *   [A] "ADR-1422: float_vif_sycl computes the CPU's arithmetic without an
+ *       fp64 type and returns its scores bit for bit", Context and Decision;
+ *   [B] "ADR-1444: float_vif_hip runs the arithmetic of the CUDA twin from one
+ *       shared header and returns the CPU's scores bit for bit", Context and
+ *       Decision;
+ *   [C] "Research-2130: float_ssim decimation on the SYCL device", Sources
+ *       (picture_copy() sample normalisation).
+ * For every frame pair it returns vif_scale0..3: four scales of separable
+ * Gaussian filtering (taps computed at run time for (float)kernelscale) and
+ * 2x decimation with a reflect-then-clamp boundary, per-pixel statistics,
+ * two terms formed in fp64 and rounded once to fp32 before a polynomial
+ * log2, and the per-scale ratio of two sequential fp32 sums (each row left
+ * to right, then the row sums top to bottom).  Results are bit-identical to
+ * the project's CPU oracle on every input.
+ *
+ * Conventions for every entry point:
+ *  - Frames are luma planes, row-major, stride = w samples, n frames packed
+ *    back to back.  Samples are uint8 when bitdepth == 8, else uint16 (host
+ *    byte order); 9..16-bit samples are divided by 2^(bitdepth-8) ([C]).
+ *    Sample values are not validated.
+ *  - Scores are written frame-major: out[4*f + s] = vif_scale<s> of frame f.
+ *  - Functions return FVIF_OK (0) or a negative status; on error the output
+ *    contents are unspecified.  The status is also kept for
+ *    fvif_last_error().
+ *  - A context is not thread-safe; separate contexts are independent.
+ *  - All work runs on the context's CUDA stream (default: the legacy default
+ *    stream; see fvif_set_stream).
+ */
+#ifndef FVIF_H
+#define FVIF_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct fvif_ctx fvif_ctx;
+
+enum fvif_status {
+    FVIF_OK = 0,
+    FVIF_EINVAL = -1, /* invalid argument (size, bit depth, pointer, ...) */
+    FVIF_ENOMEM = -2, /* device or pinned host allocation failed */
+    FVIF_ECUDA = -3   /* a CUDA call or kernel launch failed */
+};
+
+/* Create a context for frames of w x h samples.
+ *  w, h        : 16 .. 16384 ([B] Context: frames down to 16x16 must run,
+ *                including those under 72 px whose scale-3 planes are
+ *                narrower than the filter).
+ *  bitdepth    : 8 .. 16.
+ *  kernelscale : > 0; used as a float ([A] Decision: taps for the float
+ *                value of vif_kernelscale).  Scale s uses 2r+1 taps with
+ *                r = floor(kernelscale * (2^(4-s)+1) / 2); r of scale 0 must
+ *                not exceed 64.
+ *  sigma_nsq   : > 0, finite; kept as a double ([A] Context: the noise
+ *                variance stays fp64 in the statistic).
+ * Allocates the pyramid and scratch buffers for one chunk of frames on the
+ * current CUDA device.  Returns NULL on failure; the reason is then given by
+ * fvif_last_error(NULL). */
+fvif_ctx *fvif_create(int w, int h, int bitdepth, float kernelscale,
+                      double sigma_nsq);
+
+/* Score n_frames frame pairs whose samples are in DEVICE memory (caller
+ * owned, readable for the whole call).  out: HOST memory of 4*n_frames
+ * doubles.  Synchronous: returns after out is written.  n_frames == 0 is a
+ * no-op.  Frames are processed in chunks; no host round trip inside a
+ * chunk. */
+int fvif_score(fvif_ctx *ctx, const void *ref, const void *dist, int n_frames,
+               double *out);
+
+/* Same as fvif_score, but out is DEVICE memory of 4*n_frames doubles and the
+ * call only enqueues work on the context stream (it returns before the
+ * scores exist).  Inputs must stay valid until that stream reaches the end
+ * of the enqueued work. */
+int fvif_score_async(fvif_ctx *ctx, const void *ref, const void *dist,
+                     int n_frames, double *out);
+
+/* Score frame pairs whose samples are in HOST memory.  The library copies
+ * chunks to the device on its own copy stream while earlier chunks are
+ * scored (page-locked inputs overlap copy and compute; pageable ones still
+ * work, slower).  out: HOST memory of 4*n_frames doubles.  Synchronous. */
+int fvif_score_host(fvif_ctx *ctx, const void *ref, const void *dist,
+                    int n_frames, double *out);
+
+/* Free the context and everything it allocated.  NULL is a no-op. */
+void fvif_destroy(fvif_ctx *ctx);
+
+/* Run the context's work on cuda_stream (a cudaStream_t, or NULL for the
+ * legacy default stream).  The stream stays owned by the caller. */
+int fvif_set_stream(fvif_ctx *ctx, void *cuda_stream);
+
+/* Status of the last call on ctx, or with ctx == NULL of the last
+ * fvif_create on the calling thread. */
+int fvif_last_error(const fvif_ctx *ctx);
+
+/* Static text for a status code. */
+const char *fvif_strerror(int status);
+
+/* Number of frames the context scores per chunk. */
+int fvif_chunk_frames(const fvif_ctx *ctx);
+
+/* Copy the fp32 taps of scale s (0..3) into taps[0..cap); returns the tap
+ * count, or a negative status. */
+int fvif_get_taps(const fvif_ctx *ctx, int scale, float *taps, int cap);
+
+/* Diagnostics for one frame pair (device inputs, host outputs), used to
+ * localise a mismatch to one step.
+ *  planes : the ref and dist planes of scales 0..3 as fp32, in the order
+ *           ref0 dist0 ref1 dist1 ... (sum over s of 2 * w_s * h_s floats);
+ *           may be NULL.
+ *  rows   : per scale, the fp32 (num, den) sum of every row, scales one after
+ *           another (sum over s of 2 * h_s floats); may be NULL.
+ *  sums   : per scale the fp32 num and den totals (8 floats); may be NULL. */
+int fvif_debug_frame(fvif_ctx *ctx, const void *ref, const void *dist,
+                     float *planes, float *rows, float *sums);
+
+/* Kernel kinds for the profiling counters. */
+enum fvif_kernel_kind {
+    FVIF_K_DECIMATE = 0, /* the three decimation launches of a chunk      */
+    FVIF_K_STATS0 = 1,   /* the scale-0 statistic launch of a chunk       */
+    FVIF_K_STATS123 = 2, /* the scale-1..3 statistic launches of a chunk  */
+    FVIF_K_FINAL = 3,    /* the per-(frame, scale) final reduction        */
+    FVIF_K_COUNT = 4
+};
+
+/* Opt-in per-kernel timing on the launching stream: while enabled, every
+ * launch is bracketed by two CUDA events (the work itself is unchanged).
+ * Enabling clears the counters. */
+int fvif_profile_enable(fvif_ctx *ctx, int enable);
+
+/* Total device time (ms, from the events) and launch count of one kernel
+ * kind since profiling was enabled.  Waits for the recorded work to finish.
+ * Launch counts are kept even when timing is disabled. */
+int fvif_profile_read(fvif_ctx *ctx, int kind, double *total_ms,
+                      long long *launches);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FVIF_H */

@@ -15,6 +15,7 @@ from __future__ import annotations
 import ctypes
 import os
 import subprocess
+import tempfile
 import threading
 from concurrent.futures import ThreadPoolExecutor
 
@@ -52,9 +53,9 @@ def build(force: bool = False) -> str:
 def build_variant(source_text: str, tag: str) -> ctypes.CDLL:
     """Compile an edited copy of the oracle source (used by tests that plant
     a mistake in the oracle and check that a pin catches it)."""
-    os.makedirs(_OUT_DIR, exist_ok=True)
-    src = os.path.join(_OUT_DIR, "variant_%s.c" % tag)
-    so = os.path.join(_OUT_DIR, "libvariant_%s.so" % tag)
+    d = tempfile.mkdtemp(prefix="oracle_variant_")
+    src = os.path.join(d, "variant_%s.c" % tag)
+    so = os.path.join(d, "libvariant_%s.so" % tag)
     with open(src, "w") as f:
         f.write(source_text)
     subprocess.run(["gcc", *CFLAGS, "-I", _HERE, "-o", so, src, "-lm"],

@@ -1,0 +1,233 @@
+"""The CUDA library against the oracle, bit for bit, through the C ABI.
+
+Bar: every score equal to the oracle's bits (the target is identity; the
+pages' parity gate of 5e-5 is the acceptance bound and is reported when a
+value differs).  Cases: every workload that the oracle finishes in seconds,
+in full; the 4K workloads at full size in the launch configuration the
+benchmark times, on sampled frames; edge frame sizes, bit depths,
+kernelscales (fixed-width and run-time-width kernels), noise variances,
+degenerate content, every API entry point and the per-step diagnostics.
+"""
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from gpu_util import assert_bitwise, oracle_scores, to_device, torch_mod
+from vmaf_float_vif_gb300 import synthetic as S
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def fv():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import vmaf_float_vif_gb300 as fv
+    fv.build()
+    L = fv.lib()
+    assert os.path.realpath(L._name) == os.path.realpath(fv._build.LIB_PATH)
+    return fv
+
+
+def gpu_scores(fv, case, ref, dist, ks, nsq):
+    with fv.Context(case.w, case.h, case.bitdepth, ks, nsq) as ctx:
+        return ctx.score(to_device(ref), to_device(dist))
+
+
+SMALL_CASES = ["c1_576x324_8b", "c2_checker_1px_10b", "c2_checker_10px_10b",
+               "c2_edge_40x40_8b", "c2_edge_56x56_8b", "c2_edge_64x64_8b",
+               "c2_edge_71x71_8b", "c3_bright_1080p_16b"]
+
+
+@pytest.mark.parametrize("name", SMALL_CASES)
+@pytest.mark.parametrize("ks", [0.5, 1.0, 2.0])
+def test_workload_cases_bit_identical(fv, name, ks):
+    case = S.CASES[name]
+    ref, dist = case.batch(range(case.frames))
+    got = gpu_scores(fv, case, ref, dist, ks, case.nsq)
+    want = oracle_scores(ref, dist, case.bitdepth, ks, case.nsq)
+    assert_bitwise(got, want, "%s ks=%g" % (name, ks))
+
+
+def test_4k_8bit_full_clip_sampled(fv):
+    """All 20 frames of the 8-bit 4K clip in one call (two chunks); sampled
+    frames checked against the oracle one by one."""
+    case = S.CASES["c4_4k_8b"]
+    ref, dist = case.batch(range(case.frames))
+    got = gpu_scores(fv, case, ref, dist, 1.0, case.nsq)
+    for f in (0, 15, 16, 19):
+        want = oracle.frame(ref[f], dist[f], 8, 1.0, case.nsq)
+        assert_bitwise(got[f], want, "c4 frame %d" % f)
+
+
+_STREAM = {}
+
+
+def c5_stream():
+    if "c5" not in _STREAM:
+        case = S.CASES["c5_4k_10b"]
+        _STREAM["c5"] = S.streamed_batch(case, case.frames)
+    return _STREAM["c5"]
+
+
+@pytest.mark.parametrize("ks", [0.5, 1.0, 2.0])
+def test_4k_10bit_stream_sampled(fv, ks):
+    """The 240-frame 10-bit 4K stream in the benchmark's launch
+    configuration (device inputs, one fvif_score_async call, chunks of 16);
+    sampled frames against the oracle."""
+    torch = torch_mod()
+    case = S.CASES["c5_4k_10b"]
+    ref, dist = c5_stream()
+    r, d = to_device(ref), to_device(dist)
+    out = torch.empty(4 * case.frames, dtype=torch.float64, device="cuda")
+    with fv.Context(case.w, case.h, case.bitdepth, ks, case.nsq) as ctx:
+        assert ctx.chunk_frames == 16
+        ctx.score_async(r, d, out)
+        torch.cuda.synchronize()
+    got = out.cpu().numpy().reshape(-1, 4)
+    samples = [0, 17, 128, 239]
+    want = oracle_scores(ref[samples], dist[samples], 10, ks, case.nsq)
+    assert_bitwise(got[samples], want, "c5 ks=%g" % ks)
+    assert np.all((got > 0) & (got <= 1.0 + 1e-6))
+
+
+EDGE_SIZES = [(16, 16), (17, 17), (16, 40), (40, 16), (71, 71), (72, 72),
+              (129, 33), (200, 17), (1000, 16), (16, 300), (257, 130)]
+
+
+@pytest.mark.parametrize("w,h", EDGE_SIZES)
+def test_edge_sizes(fv, w, h):
+    case = S.custom_noise_case(w, h, 8, frames=2)
+    ref, dist = case.batch(range(2))
+    for ks in (0.5, 1.0, 2.0):
+        got = gpu_scores(fv, case, ref, dist, ks, 2.0)
+        want = oracle_scores(ref, dist, 8, ks, 2.0)
+        assert_bitwise(got, want, "%dx%d ks=%g" % (w, h, ks))
+
+
+@pytest.mark.parametrize("bd", [9, 10, 12, 16])
+def test_bit_depths(fv, bd):
+    case = S.custom_noise_case(180, 100, bd, frames=2)
+    ref, dist = case.batch(range(2))
+    got = gpu_scores(fv, case, ref, dist, 1.0, 2.0)
+    want = oracle_scores(ref, dist, bd, 1.0, 2.0)
+    assert_bitwise(got, want, "bitdepth %d" % bd)
+
+
+@pytest.mark.parametrize("ks", [0.25, 0.75, 1.5, 3.0, 7.5])
+def test_runtime_width_kernelscales(fv, ks):
+    """Kernelscales whose widths have no specialised kernel."""
+    case = S.custom_noise_case(150, 90, 10, frames=2)
+    ref, dist = case.batch(range(2))
+    got = gpu_scores(fv, case, ref, dist, ks, 2.0)
+    want = oracle_scores(ref, dist, 10, ks, 2.0)
+    assert_bitwise(got, want, "ks=%g" % ks)
+
+
+@pytest.mark.parametrize("nsq", [0.3, 1.5, 4.7, 2.0 / 3.0, 1e-3, 1e6])
+def test_noise_variances(fv, nsq):
+    case = S.custom_noise_case(160, 96, 8, frames=2)
+    ref, dist = case.batch(range(2))
+    got = gpu_scores(fv, case, ref, dist, 1.0, nsq)
+    want = oracle_scores(ref, dist, 8, 1.0, nsq)
+    assert_bitwise(got, want, "nsq=%g" % nsq)
+
+
+def test_degenerate_content(fv):
+    w, h = 96, 64
+    z = np.zeros((h, w), np.uint8)
+    top = np.full((h, w), 255, np.uint8)
+    rng = np.random.default_rng(5)
+    noise = rng.integers(0, 256, (h, w)).astype(np.uint8)
+    pairs = [(z, z), (top, top), (z, top), (noise, noise), (noise, z),
+             (z, noise), (top, noise)]
+    ref = np.stack([p[0] for p in pairs])
+    dist = np.stack([p[1] for p in pairs])
+    case = S.Case("degenerate", w, h, 8, len(pairs), lambda f: pairs[f])
+    got = gpu_scores(fv, case, ref, dist, 1.0, 2.0)
+    want = oracle_scores(ref, dist, 8, 1.0, 2.0)
+    assert_bitwise(got, want, "degenerate")
+    assert np.all(got[0] == 1.0)
+
+
+def test_taps_equal_oracle(fv):
+    for ks in (0.25, 0.5, 0.75, 1.0, 1.5, 2.0, 3.0, 7.5):
+        with fv.Context(64, 64, 8, ks, 2.0) as ctx:
+            for s in range(4):
+                got = ctx.taps(s)
+                want = oracle.taps(ks, s)
+                assert got.tobytes() == want.tobytes(), (ks, s)
+
+
+def test_debug_frame_matches_every_step(fv):
+    case = S.custom_noise_case(203, 77, 10, frames=1)
+    ref, dist = case.pair(0)
+    for ks in (0.5, 1.0, 2.0, 1.5):
+        with fv.Context(case.w, case.h, 10, ks, 2.0) as ctx:
+            got = ctx.debug_frame(to_device(ref), to_device(dist))
+        want = oracle.frame(ref, dist, 10, ks, 2.0, detail=True)
+        for s in range(4):
+            for q in range(2):
+                assert got["planes"][s][q].tobytes() == \
+                    want["planes"][s][q].tobytes(), ("plane", ks, s, q)
+            assert got["rows"][s].tobytes() == want["rows"][s].tobytes(), \
+                ("rows", ks, s)
+        assert got["sums"].tobytes() == want["sums"].tobytes(), ("sums", ks)
+
+
+def test_entry_points_agree(fv):
+    """fvif_score, fvif_score_async (on a side stream) and fvif_score_host
+    (pinned and pageable inputs) return the same bits; 37 frames make a
+    ragged last chunk."""
+    torch = torch_mod()
+    case = S.custom_noise_case(300, 170, 12, frames=37)
+    ref, dist = case.batch(range(case.frames))
+    want = oracle_scores(ref, dist, 12, 1.0, 2.0)
+    with fv.Context(case.w, case.h, 12, 1.0, 2.0) as ctx:
+        assert_bitwise(ctx.score(to_device(ref), to_device(dist)), want,
+                       "score")
+        side = torch.cuda.Stream()
+        out = torch.zeros(4 * case.frames, dtype=torch.float64, device="cuda")
+        r, d = to_device(ref), to_device(dist)
+        torch.cuda.synchronize()
+        ctx.set_stream(side)
+        ctx.score_async(r, d, out)
+        side.synchronize()
+        assert_bitwise(out.cpu().numpy().reshape(-1, 4), want, "async")
+        ctx.set_stream(None)
+        assert_bitwise(ctx.score_host(ref, dist), want, "host pageable")
+        pr = torch.from_numpy(ref.view(np.int16)).pin_memory()
+        pd = torch.from_numpy(dist.view(np.int16)).pin_memory()
+        got = ctx.score_host(pr.numpy().view(np.uint16),
+                             pd.numpy().view(np.uint16))
+        assert_bitwise(got, want, "host pinned")
+        # repeated calls reuse the buffers and keep the bits
+        assert_bitwise(ctx.score_host(ref, dist), want, "host again")
+
+
+def test_zero_frames_and_bad_calls(fv):
+    torch = torch_mod()
+    with fv.Context(64, 48, 8, 1.0, 2.0) as ctx:
+        empty = torch.zeros(0, dtype=torch.uint8, device="cuda")
+        assert ctx.score(empty, empty).shape == (0, 4)
+        L = fv.lib()
+        assert L.fvif_score(ctx.handle, None, None, 2, None) == fv.FVIF_EINVAL
+        assert L.fvif_score(ctx.handle, None, None, -1, None) == fv.FVIF_EINVAL
+        assert L.fvif_last_error(ctx.handle) == fv.FVIF_EINVAL
+        with pytest.raises(TypeError):
+            ctx.score(torch.zeros(64 * 48, dtype=torch.int16, device="cuda"),
+                      torch.zeros(64 * 48, dtype=torch.int16, device="cuda"))
+
+
+def test_chunk_size_override(fv, monkeypatch):
+    """A context made with FVIF_CHUNK=3 splits 8 frames into 3+3+2."""
+    monkeypatch.setenv("FVIF_CHUNK", "3")
+    case = S.custom_noise_case(90, 60, 8, frames=8)
+    ref, dist = case.batch(range(8))
+    with fv.Context(case.w, case.h, 8, 1.0, 2.0) as ctx:
+        assert ctx.chunk_frames == 3
+        got = ctx.score(to_device(ref), to_device(dist))
+    assert_bitwise(got, oracle_scores(ref, dist, 8, 1.0, 2.0), "chunk 3")

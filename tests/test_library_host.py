@@ -1,0 +1,84 @@
+"""libfvif.so on the host, without a GPU: it builds for sm_103a, loads,
+exports every entry point include/fvif.h declares, and rejects invalid
+arguments before any CUDA call."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import vmaf_float_vif_gb300 as fv
+from vmaf_float_vif_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fvif.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fvif_[a-z_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    fv.build()
+    return fv.lib()
+
+
+def test_header_matches_binding_list():
+    assert declared_functions() == sorted(_lib.EXPORTS)
+
+
+def test_every_declared_symbol_is_exported(L):
+    out = subprocess.run(["nm", "-D", "--defined-only", fv._build.LIB_PATH],
+                         check=True, capture_output=True, text=True).stdout
+    exported = set(line.split()[-1] for line in out.splitlines() if line)
+    for name in declared_functions():
+        assert name in exported, name
+        assert getattr(L, name) is not None
+
+
+def test_library_targets_sm103a_only():
+    assert fv._build.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
+    assert "--fmad=false" in fv._build.NVCC_FLAGS
+
+
+@pytest.mark.parametrize("args", [
+    (15, 64, 8, 1.0, 2.0), (64, 15, 8, 1.0, 2.0), (16385, 64, 8, 1.0, 2.0),
+    (64, 64, 7, 1.0, 2.0), (64, 64, 17, 1.0, 2.0), (64, 64, 8, 0.0, 2.0),
+    (64, 64, 8, -1.0, 2.0), (64, 64, 8, float("nan"), 2.0),
+    (64, 64, 8, 1.0, 0.0), (64, 64, 8, 1.0, -2.0),
+    (64, 64, 8, 1.0, float("inf")), (64, 64, 8, 8.0, 2.0),
+])
+def test_create_rejects_invalid_arguments(L, args):
+    ctx = L.fvif_create(*args)
+    assert not ctx
+    assert L.fvif_last_error(None) == fv.FVIF_EINVAL
+
+
+def test_null_context_calls(L):
+    for name in ("fvif_score", "fvif_score_async", "fvif_score_host"):
+        assert getattr(L, name)(None, None, None, 1, None) == fv.FVIF_EINVAL
+    assert L.fvif_set_stream(None, None) == fv.FVIF_EINVAL
+    assert L.fvif_chunk_frames(None) == fv.FVIF_EINVAL
+    buf = (ctypes.c_float * 8)()
+    assert L.fvif_get_taps(None, 0, buf, 8) == fv.FVIF_EINVAL
+    assert L.fvif_debug_frame(None, None, None, None, None, None) == \
+        fv.FVIF_EINVAL
+    L.fvif_destroy(None)  # NULL-safe
+
+
+def test_strerror(L):
+    assert L.fvif_strerror(0) == b"ok"
+    assert L.fvif_strerror(-1) == b"invalid argument"
+    assert L.fvif_strerror(-2) == b"out of memory"
+    assert L.fvif_strerror(-3) == b"CUDA error"
+    assert L.fvif_strerror(99) == b"unknown status"
+
+
+def test_missing_library_raises(monkeypatch, tmp_path):
+    monkeypatch.setattr(_lib, "_lib", None)
+    with pytest.raises(RuntimeError, match="not built"):
+        _lib.lib(str(tmp_path / "nope.so"))

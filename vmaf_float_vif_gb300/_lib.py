@@ -1,0 +1,350 @@
+"""ctypes binding of libfvif.so (argument marshalling only).
+
+The shared library is loaded on first use.  If it is missing, cannot be
+loaded, or has no usable GPU, the calls raise: there is deliberately no
+fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional, Tuple
+
+import numpy as np
+
+from . import _build
+
+FVIF_OK = 0
+FVIF_EINVAL = -1
+FVIF_ENOMEM = -2
+FVIF_ECUDA = -3
+
+# Every symbol include/fvif.h declares.
+EXPORTS = (
+    "fvif_create", "fvif_score", "fvif_score_async", "fvif_score_host",
+    "fvif_destroy", "fvif_set_stream", "fvif_last_error", "fvif_strerror",
+    "fvif_chunk_frames", "fvif_get_taps", "fvif_debug_frame",
+    "fvif_profile_enable", "fvif_profile_read",
+)
+
+FVIF_K_DECIMATE, FVIF_K_STATS0, FVIF_K_STATS123, FVIF_K_FINAL = range(4)
+KERNEL_KINDS = {"decimate": 0, "stats_scale0": 1, "stats_scale123": 2,
+                "final": 3}
+
+_lock = threading.Lock()
+_lib: Optional[ctypes.CDLL] = None
+
+
+class FvifError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__("%s failed: %s (status %d)" %
+                         (what, _strerror_safe(status), status))
+
+
+def _strerror_safe(status: int) -> str:
+    try:
+        return lib().fvif_strerror(status).decode()
+    except Exception:  # library itself unavailable
+        return {0: "ok", -1: "invalid argument", -2: "out of memory",
+                -3: "CUDA error"}.get(status, "unknown status")
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    return _build.build(force=force, verbose=verbose)
+
+
+def _declare(L: ctypes.CDLL) -> ctypes.CDLL:
+    vp, i, f, d = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_double
+    fp = ctypes.POINTER(ctypes.c_float)
+    dp = ctypes.POINTER(ctypes.c_double)
+    L.fvif_create.argtypes = [i, i, i, f, d]
+    L.fvif_create.restype = vp
+    for name in ("fvif_score", "fvif_score_async", "fvif_score_host"):
+        fn = getattr(L, name)
+        fn.argtypes = [vp, vp, vp, i, vp]
+        fn.restype = i
+    L.fvif_destroy.argtypes = [vp]
+    L.fvif_destroy.restype = None
+    L.fvif_set_stream.argtypes = [vp, vp]
+    L.fvif_set_stream.restype = i
+    L.fvif_last_error.argtypes = [vp]
+    L.fvif_last_error.restype = i
+    L.fvif_strerror.argtypes = [i]
+    L.fvif_strerror.restype = ctypes.c_char_p
+    L.fvif_chunk_frames.argtypes = [vp]
+    L.fvif_chunk_frames.restype = i
+    L.fvif_get_taps.argtypes = [vp, i, fp, i]
+    L.fvif_get_taps.restype = i
+    L.fvif_debug_frame.argtypes = [vp, vp, vp, fp, fp, fp]
+    L.fvif_debug_frame.restype = i
+    L.fvif_profile_enable.argtypes = [vp, i]
+    L.fvif_profile_enable.restype = i
+    L.fvif_profile_read.argtypes = [vp, i, dp, ctypes.POINTER(ctypes.c_longlong)]
+    L.fvif_profile_read.restype = i
+    return L
+
+
+def lib(path: Optional[str] = None) -> ctypes.CDLL:
+    """Load libfvif.so (built in-tree by ``build()``)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            p = path or _build.LIB_PATH
+            if not os.path.exists(p):
+                raise RuntimeError(
+                    "libfvif.so is not built (%s); run "
+                    "vmaf_float_vif_gb300.build() first" % p)
+            _lib = _declare(ctypes.CDLL(p))
+        return _lib
+
+
+# ---------------------------------------------------------------------------
+# buffer helpers
+
+
+def _dev_ptr(t, bitdepth: int, what: str) -> int:
+    import torch
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError("%s must be a CUDA tensor" % what)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % what)
+    want = 1 if bitdepth == 8 else 2
+    if t.element_size() != want:
+        raise TypeError("%s: %d-bit samples need %d-byte elements, got %s"
+                        % (what, bitdepth, want, t.dtype))
+    return t.data_ptr()
+
+
+def _host_array(a, bitdepth: int, what: str) -> np.ndarray:
+    try:
+        import torch
+        if isinstance(a, torch.Tensor):
+            if a.is_cuda:
+                raise TypeError("%s must be host memory" % what)
+            a = a.numpy()
+    except ImportError:
+        pass
+    dt = np.uint8 if bitdepth == 8 else np.uint16
+    if not isinstance(a, np.ndarray) or a.dtype != dt:
+        raise TypeError("%s must be a %s array" % (what, np.dtype(dt).name))
+    if not a.flags["C_CONTIGUOUS"]:
+        raise ValueError("%s must be C-contiguous" % what)
+    return a
+
+
+def _frames(a, w: int, h: int) -> int:
+    n_elems = int(np.prod(a.shape)) if len(a.shape) else 0
+    if n_elems % (w * h):
+        raise ValueError("buffer is not a whole number of %dx%d frames" % (w, h))
+    return n_elems // (w * h)
+
+
+# ---------------------------------------------------------------------------
+# the C entry points, by name
+
+
+def fvif_create(w: int, h: int, bitdepth: int, kernelscale: float,
+                sigma_nsq: float) -> int:
+    L = lib()
+    ctx = L.fvif_create(int(w), int(h), int(bitdepth), float(kernelscale),
+                        float(sigma_nsq))
+    if not ctx:
+        raise FvifError(L.fvif_last_error(None), "fvif_create")
+    return ctx
+
+
+def fvif_destroy(ctx: int) -> None:
+    lib().fvif_destroy(ctx)
+
+
+def fvif_set_stream(ctx: int, stream) -> None:
+    handle = getattr(stream, "cuda_stream", stream)
+    st = lib().fvif_set_stream(ctx, handle or None)
+    if st:
+        raise FvifError(st, "fvif_set_stream")
+
+
+def fvif_last_error(ctx: Optional[int]) -> int:
+    return lib().fvif_last_error(ctx)
+
+
+def fvif_strerror(status: int) -> str:
+    return lib().fvif_strerror(int(status)).decode()
+
+
+def fvif_chunk_frames(ctx: int) -> int:
+    return lib().fvif_chunk_frames(ctx)
+
+
+def fvif_get_taps(ctx: int, scale: int) -> np.ndarray:
+    buf = np.zeros(129, np.float32)
+    n = lib().fvif_get_taps(ctx, int(scale),
+                            buf.ctypes.data_as(ctypes.POINTER(ctypes.c_float)),
+                            buf.size)
+    if n < 0:
+        raise FvifError(n, "fvif_get_taps")
+    return buf[:n].copy()
+
+
+def fvif_score(ctx: int, ref, dist, w: int, h: int, bitdepth: int) -> np.ndarray:
+    """Device inputs (CUDA tensors), host results of shape (n, 4)."""
+    n = _frames(ref, w, h)
+    if _frames(dist, w, h) != n:
+        raise ValueError("ref and dist hold different frame counts")
+    out = np.zeros((n, 4), np.float64)
+    st = lib().fvif_score(ctx, _dev_ptr(ref, bitdepth, "ref"),
+                          _dev_ptr(dist, bitdepth, "dist"), n,
+                          out.ctypes.data)
+    if st:
+        raise FvifError(st, "fvif_score")
+    return out
+
+
+def fvif_score_async(ctx: int, ref, dist, out, w: int, h: int,
+                     bitdepth: int) -> None:
+    """Device inputs and a device float64 output of 4*n values; enqueues only."""
+    import torch
+    n = _frames(ref, w, h)
+    if _frames(dist, w, h) != n:
+        raise ValueError("ref and dist hold different frame counts")
+    if (not isinstance(out, torch.Tensor) or not out.is_cuda or
+            out.dtype != torch.float64 or out.numel() < 4 * n or
+            not out.is_contiguous()):
+        raise TypeError("out must be a contiguous CUDA float64 tensor of "
+                        ">= 4*n values")
+    st = lib().fvif_score_async(ctx, _dev_ptr(ref, bitdepth, "ref"),
+                                _dev_ptr(dist, bitdepth, "dist"), n,
+                                out.data_ptr())
+    if st:
+        raise FvifError(st, "fvif_score_async")
+
+
+def fvif_score_host(ctx: int, ref, dist, w: int, h: int,
+                    bitdepth: int) -> np.ndarray:
+    """Host inputs (numpy arrays or CPU tensors, ideally page-locked), host
+    results of shape (n, 4)."""
+    r = _host_array(ref, bitdepth, "ref")
+    d = _host_array(dist, bitdepth, "dist")
+    n = _frames(r, w, h)
+    if _frames(d, w, h) != n:
+        raise ValueError("ref and dist hold different frame counts")
+    out = np.zeros((n, 4), np.float64)
+    st = lib().fvif_score_host(ctx, r.ctypes.data, d.ctypes.data, n,
+                               out.ctypes.data)
+    if st:
+        raise FvifError(st, "fvif_score_host")
+    return out
+
+
+def plane_sizes(w: int, h: int):
+    out = [(w, h)]
+    for _ in range(3):
+        w, h = w // 2, h // 2
+        out.append((w, h))
+    return out
+
+
+def fvif_debug_frame(ctx: int, ref, dist, w: int, h: int, bitdepth: int):
+    """Planes, row sums and per-scale sums of one frame pair (device inputs)."""
+    sizes = plane_sizes(w, h)
+    planes = np.zeros(sum(2 * a * b for a, b in sizes), np.float32)
+    rows = np.zeros(sum(2 * b for _, b in sizes), np.float32)
+    sums = np.zeros(8, np.float32)
+    fp = ctypes.POINTER(ctypes.c_float)
+    st = lib().fvif_debug_frame(ctx, _dev_ptr(ref, bitdepth, "ref"),
+                                _dev_ptr(dist, bitdepth, "dist"),
+                                planes.ctypes.data_as(fp),
+                                rows.ctypes.data_as(fp),
+                                sums.ctypes.data_as(fp))
+    if st:
+        raise FvifError(st, "fvif_debug_frame")
+    out = {"planes": [], "rows": [], "sums": sums.reshape(4, 2)}
+    po = ro = 0
+    for ws, hs in sizes:
+        n = ws * hs
+        out["planes"].append((planes[po:po + n].reshape(hs, ws),
+                              planes[po + n:po + 2 * n].reshape(hs, ws)))
+        po += 2 * n
+        out["rows"].append(rows[ro:ro + 2 * hs].reshape(hs, 2))
+        ro += 2 * hs
+    return out
+
+
+def fvif_profile_enable(ctx: int, enable: bool) -> None:
+    st = lib().fvif_profile_enable(ctx, 1 if enable else 0)
+    if st:
+        raise FvifError(st, "fvif_profile_enable")
+
+
+def fvif_profile_read(ctx: int, kind: int):
+    """(total device ms, launch count) of one kernel kind."""
+    ms = ctypes.c_double()
+    n = ctypes.c_longlong()
+    st = lib().fvif_profile_read(ctx, int(kind), ctypes.byref(ms),
+                                 ctypes.byref(n))
+    if st:
+        raise FvifError(st, "fvif_profile_read")
+    return ms.value, n.value
+
+
+class Context:
+    """Owning wrapper: ``with Context(w, h, bd, ks, nsq) as c: c.score(...)``."""
+
+    def __init__(self, w: int, h: int, bitdepth: int, kernelscale: float = 1.0,
+                 sigma_nsq: float = 2.0):
+        self.w, self.h, self.bitdepth = int(w), int(h), int(bitdepth)
+        self.kernelscale, self.sigma_nsq = float(kernelscale), float(sigma_nsq)
+        self.handle = fvif_create(self.w, self.h, self.bitdepth,
+                                  self.kernelscale, self.sigma_nsq)
+
+    def close(self) -> None:
+        if self.handle:
+            fvif_destroy(self.handle)
+            self.handle = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def set_stream(self, stream) -> None:
+        fvif_set_stream(self.handle, stream)
+
+    def score(self, ref, dist) -> np.ndarray:
+        return fvif_score(self.handle, ref, dist, self.w, self.h, self.bitdepth)
+
+    def score_async(self, ref, dist, out) -> None:
+        fvif_score_async(self.handle, ref, dist, out, self.w, self.h,
+                         self.bitdepth)
+
+    def score_host(self, ref, dist) -> np.ndarray:
+        return fvif_score_host(self.handle, ref, dist, self.w, self.h,
+                               self.bitdepth)
+
+    def taps(self, scale: int) -> np.ndarray:
+        return fvif_get_taps(self.handle, scale)
+
+    def debug_frame(self, ref, dist):
+        return fvif_debug_frame(self.handle, ref, dist, self.w, self.h,
+                                self.bitdepth)
+
+    def profile(self, enable: bool = True) -> None:
+        fvif_profile_enable(self.handle, enable)
+
+    def profile_read(self):
+        """{kind name: (total ms, launches)}"""
+        return {k: fvif_profile_read(self.handle, v)
+                for k, v in KERNEL_KINDS.items()}
+
+    @property
+    def chunk_frames(self) -> int:
+        return fvif_chunk_frames(self.handle)

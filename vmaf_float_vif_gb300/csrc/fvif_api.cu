@@ -1,0 +1,655 @@
+/*
+ * fvif_api.cu -- host side of libfvif: context, taps, chunked launches and
+ * the C ABI declared in include/fvif.h.
+ */
+#include <cmath>
+#include <cstdio>
+#include <vector>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+
+#include "../../include/fvif.h"
+#include "fvif_internal.h"
+
+using namespace fvif;
+
+namespace {
+
+constexpr int kDefaultChunk = 16;
+
+thread_local int g_create_status = FVIF_OK;
+
+/* Taps of scale s for kernelscale ks.  "ADR-1422: float_vif_sycl computes
+ * the CPU's arithmetic without an fp64 type ...", Decision: the taps are the
+ * CPU routine's, computed at run time for (float)vif_kernelscale and handed
+ * to every launch by value.  The routine is the VIF Gaussian: base window
+ * B = 2^(4-s)+1, sigma = ks B / 5, half-width r = floor(ks B / 2), weights
+ * exp(-d^2 / (2 sigma^2)) in fp64 normalised by their fp64 sum (ascending),
+ * each rounded to fp32.                                                     */
+int make_taps(float kernelscale, int s, Taps &out)
+{
+    const double ks = (double)kernelscale;
+    const double base = (double)((1 << (4 - s)) + 1);
+    const double half = std::floor(ks * base / 2.0);
+    if (!(half >= 0.0) || half > (double)kMaxRadius)
+        return FVIF_EINVAL;
+    const int r = (int)half;
+    std::memset(&out, 0, sizeof out);
+    out.n = 2 * r + 1;
+    if (r == 0) {
+        out.t[0] = 1.0f;
+        return FVIF_OK;
+    }
+    const double sigma = ks * base / 5.0;
+    const double two_sigma_sq = 2.0 * sigma * sigma;
+    double wk[kMaxTaps];
+    double sum = 0.0;
+    for (int k = 0; k < out.n; ++k) {
+        const double d = (double)(k - r);
+        wk[k] = std::exp(-(d * d) / two_sigma_sq);
+        sum = sum + wk[k];
+    }
+    for (int k = 0; k < out.n; ++k)
+        out.t[k] = (float)(wk[k] / sum);
+    return FVIF_OK;
+}
+
+/* Keeps the caller's current device; switches to the context's for the
+ * duration of one API call. */
+struct DeviceGuard {
+    int prev = -1;
+    bool ok = false;
+    explicit DeviceGuard(int dev)
+    {
+        if (cudaGetDevice(&prev) != cudaSuccess)
+            return;
+        ok = (prev == dev) || (cudaSetDevice(dev) == cudaSuccess);
+    }
+    ~DeviceGuard()
+    {
+        int cur = -1;
+        if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev)
+            cudaSetDevice(prev);
+    }
+};
+
+} // namespace
+
+struct fvif_ctx {
+    int w = 0, h = 0, bitdepth = 8;
+    float kernelscale = 1.0f;
+    double nsq = 2.0;
+    float gain_limit = 100.0f;
+    int ws[kScales] = {}, hs[kScales] = {};
+    Taps taps[kScales];
+    int chunk = kDefaultChunk;
+    int device = 0;
+    cudaStream_t stream = nullptr;
+    int last_status = FVIF_OK;
+
+    float2 *pyr[kScales] = {};   /* scales 1..3, chunk frames each        */
+    float2 *rows = nullptr;      /* chunk frames x sum(h_s) (num, den)    */
+    int rows_stride = 0;
+    int rows_base[kScales] = {};
+    float2 *sums = nullptr;      /* chunk x 4 (diagnostics)               */
+
+    double *d_out = nullptr;     /* results of the synchronous calls      */
+    double *h_out = nullptr;     /* pinned staging of d_out               */
+    int out_cap = 0;
+
+    /* opt-in launch timing: event pairs per kernel kind */
+    bool profiling = false;
+    std::vector<cudaEvent_t> prof_events[FVIF_K_COUNT];
+    size_t prof_used[FVIF_K_COUNT] = {};
+    long long launches[FVIF_K_COUNT] = {};
+
+    /* host-input pipeline (allocated on first fvif_score_host) */
+    unsigned char *stage[2] = {};
+    cudaStream_t copy_stream = nullptr;
+    cudaEvent_t copied[2] = {};
+    cudaEvent_t consumed[2] = {};
+
+    size_t sample_bytes() const { return bitdepth == 8 ? 1u : 2u; }
+    size_t frame_bytes() const { return (size_t)w * h * sample_bytes(); }
+};
+
+namespace {
+
+int set_status(fvif_ctx *ctx, int st)
+{
+    if (ctx)
+        ctx->last_status = st;
+    return st;
+}
+
+int cuda_status(cudaError_t e)
+{
+    if (e == cudaSuccess)
+        return FVIF_OK;
+    if (e == cudaErrorMemoryAllocation)
+        return FVIF_ENOMEM;
+    return FVIF_ECUDA;
+}
+
+void release(fvif_ctx *c)
+{
+    for (int s = 0; s < kScales; ++s)
+        if (c->pyr[s])
+            cudaFree(c->pyr[s]);
+    if (c->rows)
+        cudaFree(c->rows);
+    if (c->sums)
+        cudaFree(c->sums);
+    if (c->d_out)
+        cudaFree(c->d_out);
+    if (c->h_out)
+        cudaFreeHost(c->h_out);
+    for (int i = 0; i < 2; ++i) {
+        if (c->stage[i])
+            cudaFree(c->stage[i]);
+        if (c->copied[i])
+            cudaEventDestroy(c->copied[i]);
+        if (c->consumed[i])
+            cudaEventDestroy(c->consumed[i]);
+    }
+    if (c->copy_stream)
+        cudaStreamDestroy(c->copy_stream);
+    for (int k = 0; k < FVIF_K_COUNT; ++k)
+        for (cudaEvent_t ev : c->prof_events[k])
+            cudaEventDestroy(ev);
+}
+
+/* Record the start event of one launch of kind k (profiling only). */
+cudaError_t prof_begin(fvif_ctx *c, int k)
+{
+    c->launches[k] += 1;
+    if (!c->profiling)
+        return cudaSuccess;
+    std::vector<cudaEvent_t> &v = c->prof_events[k];
+    if (c->prof_used[k] + 2 > v.size()) {
+        for (int i = 0; i < 2; ++i) {
+            cudaEvent_t ev;
+            cudaError_t e = cudaEventCreate(&ev);
+            if (e != cudaSuccess)
+                return e;
+            v.push_back(ev);
+        }
+    }
+    return cudaEventRecord(v[c->prof_used[k]], c->stream);
+}
+
+cudaError_t prof_end(fvif_ctx *c, int k)
+{
+    if (!c->profiling)
+        return cudaSuccess;
+    cudaError_t e = cudaEventRecord(c->prof_events[k][c->prof_used[k] + 1],
+                                    c->stream);
+    c->prof_used[k] += 2;
+    return e;
+}
+
+SrcDesc scale0_src(const fvif_ctx *c, const void *ref, const void *dist)
+{
+    SrcDesc d;
+    d.kind = c->bitdepth == 8 ? SrcKind::U8 : SrcKind::U16;
+    d.x = ref;
+    d.y = dist;
+    d.scale = c->bitdepth == 8 ? 1.0f
+                               : std::ldexp(1.0f, -(c->bitdepth - 8));
+    d.frame_elems = (size_t)c->w * c->h;
+    return d;
+}
+
+SrcDesc pyr_src(const fvif_ctx *c, int s)
+{
+    SrcDesc d;
+    d.kind = SrcKind::F2;
+    d.x = c->pyr[s];
+    d.y = nullptr;
+    d.scale = 1.0f;
+    d.frame_elems = (size_t)c->ws[s] * c->hs[s];
+    return d;
+}
+
+/* One chunk (nf <= chunk frames) on the context stream: the pyramid, the
+ * four statistic launches and the final reduction into out (device). */
+int run_chunk(fvif_ctx *c, const void *ref, const void *dist, int nf,
+              double *out, float2 *sums)
+{
+    cudaStream_t st = c->stream;
+    const SrcDesc s0 = scale0_src(c, ref, dist);
+    cudaError_t e = cudaSuccess;
+
+    for (int s = 1; s < kScales && e == cudaSuccess; ++s) {
+        DecArgs d;
+        d.src = (s == 1) ? s0 : pyr_src(c, s - 1);
+        d.w = c->ws[s - 1];
+        d.h = c->hs[s - 1];
+        d.nframes = nf;
+        d.dst = c->pyr[s];
+        d.dst_frame_elems = (size_t)c->ws[s] * c->hs[s];
+        e = prof_begin(c, FVIF_K_DECIMATE);
+        if (e == cudaSuccess)
+            e = launch_decimate(d, c->taps[s], st);
+        if (e == cudaSuccess)
+            e = prof_end(c, FVIF_K_DECIMATE);
+    }
+    for (int s = 0; s < kScales && e == cudaSuccess; ++s) {
+        StatsArgs a;
+        a.src = (s == 0) ? s0 : pyr_src(c, s);
+        a.w = c->ws[s];
+        a.h = c->hs[s];
+        a.nframes = nf;
+        a.nsq = c->nsq;
+        a.gain_limit = c->gain_limit;
+        a.rows = c->rows;
+        a.rows_stride = c->rows_stride;
+        a.rows_base = c->rows_base[s];
+        const int kind = s == 0 ? FVIF_K_STATS0 : FVIF_K_STATS123;
+        e = prof_begin(c, kind);
+        if (e == cudaSuccess)
+            e = launch_stats(a, c->taps[s], st);
+        if (e == cudaSuccess)
+            e = prof_end(c, kind);
+    }
+    if (e == cudaSuccess) {
+        FinalArgs f;
+        f.rows = c->rows;
+        f.rows_stride = c->rows_stride;
+        for (int s = 0; s < kScales; ++s) {
+            f.rows_base[s] = c->rows_base[s];
+            f.h[s] = c->hs[s];
+        }
+        f.nframes = nf;
+        f.out = out;
+        f.sums = sums;
+        e = prof_begin(c, FVIF_K_FINAL);
+        if (e == cudaSuccess)
+            e = launch_final(f, st);
+        if (e == cudaSuccess)
+            e = prof_end(c, FVIF_K_FINAL);
+    }
+    return cuda_status(e);
+}
+
+int enqueue_all(fvif_ctx *c, const void *ref, const void *dist, int n,
+                double *out)
+{
+    const size_t fb = c->frame_bytes();
+    for (int f0 = 0; f0 < n; f0 += c->chunk) {
+        const int nf = (n - f0 < c->chunk) ? n - f0 : c->chunk;
+        const int st =
+            run_chunk(c, static_cast<const unsigned char *>(ref) + fb * f0,
+                      static_cast<const unsigned char *>(dist) + fb * f0, nf,
+                      out + (size_t)kScales * f0, nullptr);
+        if (st != FVIF_OK)
+            return st;
+    }
+    return FVIF_OK;
+}
+
+int ensure_out(fvif_ctx *c, int n)
+{
+    if (n <= c->out_cap)
+        return FVIF_OK;
+    int cap = c->out_cap ? c->out_cap : 256;
+    while (cap < n)
+        cap *= 2;
+    double *d = nullptr, *h = nullptr;
+    if (cudaMalloc(&d, sizeof(double) * kScales * (size_t)cap) != cudaSuccess)
+        return FVIF_ENOMEM;
+    if (cudaMallocHost(&h, sizeof(double) * kScales * (size_t)cap) !=
+        cudaSuccess) {
+        cudaFree(d);
+        return FVIF_ENOMEM;
+    }
+    if (c->d_out)
+        cudaFree(c->d_out);
+    if (c->h_out)
+        cudaFreeHost(c->h_out);
+    c->d_out = d;
+    c->h_out = h;
+    c->out_cap = cap;
+    return FVIF_OK;
+}
+
+int finish_to_host(fvif_ctx *c, int n, double *out)
+{
+    cudaError_t e = cudaMemcpyAsync(c->h_out, c->d_out,
+                                    sizeof(double) * kScales * (size_t)n,
+                                    cudaMemcpyDeviceToHost, c->stream);
+    if (e == cudaSuccess)
+        e = cudaStreamSynchronize(c->stream);
+    if (e != cudaSuccess)
+        return cuda_status(e);
+    std::memcpy(out, c->h_out, sizeof(double) * kScales * (size_t)n);
+    return FVIF_OK;
+}
+
+int ensure_pipeline(fvif_ctx *c)
+{
+    if (c->copy_stream)
+        return FVIF_OK;
+    const size_t slot = 2 * c->frame_bytes() * (size_t)c->chunk;
+    cudaError_t e = cudaStreamCreateWithFlags(&c->copy_stream,
+                                              cudaStreamNonBlocking);
+    for (int i = 0; i < 2 && e == cudaSuccess; ++i) {
+        e = cudaMalloc(&c->stage[i], slot);
+        if (e == cudaSuccess)
+            e = cudaEventCreateWithFlags(&c->copied[i],
+                                         cudaEventDisableTiming);
+        if (e == cudaSuccess)
+            e = cudaEventCreateWithFlags(&c->consumed[i],
+                                         cudaEventDisableTiming);
+    }
+    return cuda_status(e);
+}
+
+} // namespace
+
+extern "C" {
+
+fvif_ctx *fvif_create(int w, int h, int bitdepth, float kernelscale,
+                      double sigma_nsq)
+{
+    g_create_status = FVIF_EINVAL;
+    if (w < 16 || h < 16 || w > 16384 || h > 16384)
+        return nullptr;
+    if (bitdepth < 8 || bitdepth > 16)
+        return nullptr;
+    if (!(kernelscale > 0.0f) || !std::isfinite(kernelscale))
+        return nullptr;
+    if (!(sigma_nsq > 0.0) || !std::isfinite(sigma_nsq))
+        return nullptr;
+
+    fvif_ctx *c = new (std::nothrow) fvif_ctx();
+    if (!c) {
+        g_create_status = FVIF_ENOMEM;
+        return nullptr;
+    }
+    c->w = w;
+    c->h = h;
+    c->bitdepth = bitdepth;
+    c->kernelscale = kernelscale;
+    c->nsq = sigma_nsq;
+    for (int s = 0; s < kScales; ++s) {
+        c->ws[s] = s == 0 ? w : c->ws[s - 1] / 2;
+        c->hs[s] = s == 0 ? h : c->hs[s - 1] / 2;
+        if (make_taps(kernelscale, s, c->taps[s]) != FVIF_OK) {
+            delete c;
+            return nullptr;
+        }
+    }
+    if (const char *env = std::getenv("FVIF_CHUNK")) {
+        const int v = std::atoi(env);
+        if (v > 0 && v <= 256)
+            c->chunk = v;
+    }
+    cudaError_t e = cudaGetDevice(&c->device);
+    int rows_total = 0;
+    for (int s = 0; s < kScales; ++s) {
+        c->rows_base[s] = rows_total;
+        rows_total += c->hs[s];
+    }
+    c->rows_stride = rows_total;
+    for (int s = 1; s < kScales && e == cudaSuccess; ++s)
+        e = cudaMalloc(&c->pyr[s], sizeof(float2) * (size_t)c->ws[s] *
+                                       c->hs[s] * c->chunk);
+    if (e == cudaSuccess)
+        e = cudaMalloc(&c->rows,
+                       sizeof(float2) * (size_t)rows_total * c->chunk);
+    if (e == cudaSuccess)
+        e = cudaMalloc(&c->sums, sizeof(float2) * kScales * (size_t)c->chunk);
+    int st = cuda_status(e);
+    if (st == FVIF_OK)
+        st = ensure_out(c, c->chunk);
+    if (st != FVIF_OK) {
+        release(c);
+        delete c;
+        g_create_status = st;
+        return nullptr;
+    }
+    g_create_status = FVIF_OK;
+    return c;
+}
+
+void fvif_destroy(fvif_ctx *ctx)
+{
+    if (!ctx)
+        return;
+    DeviceGuard g(ctx->device);
+    cudaStreamSynchronize(ctx->stream);
+    release(ctx);
+    delete ctx;
+}
+
+int fvif_set_stream(fvif_ctx *ctx, void *cuda_stream)
+{
+    if (!ctx)
+        return FVIF_EINVAL;
+    ctx->stream = static_cast<cudaStream_t>(cuda_stream);
+    return set_status(ctx, FVIF_OK);
+}
+
+int fvif_last_error(const fvif_ctx *ctx)
+{
+    return ctx ? ctx->last_status : g_create_status;
+}
+
+const char *fvif_strerror(int status)
+{
+    switch (status) {
+    case FVIF_OK: return "ok";
+    case FVIF_EINVAL: return "invalid argument";
+    case FVIF_ENOMEM: return "out of memory";
+    case FVIF_ECUDA: return "CUDA error";
+    default: return "unknown status";
+    }
+}
+
+int fvif_profile_enable(fvif_ctx *ctx, int enable)
+{
+    if (!ctx)
+        return FVIF_EINVAL;
+    DeviceGuard g(ctx->device);
+    if (cudaStreamSynchronize(ctx->stream) != cudaSuccess)
+        return set_status(ctx, FVIF_ECUDA);
+    ctx->profiling = enable != 0;
+    for (int k = 0; k < FVIF_K_COUNT; ++k) {
+        ctx->prof_used[k] = 0;
+        ctx->launches[k] = 0;
+    }
+    return set_status(ctx, FVIF_OK);
+}
+
+int fvif_profile_read(fvif_ctx *ctx, int kind, double *total_ms,
+                      long long *launches)
+{
+    if (!ctx || kind < 0 || kind >= FVIF_K_COUNT || !total_ms || !launches)
+        return ctx ? set_status(ctx, FVIF_EINVAL) : FVIF_EINVAL;
+    DeviceGuard g(ctx->device);
+    double ms = 0.0;
+    const std::vector<cudaEvent_t> &v = ctx->prof_events[kind];
+    for (size_t i = 0; i + 1 < ctx->prof_used[kind]; i += 2) {
+        if (cudaEventSynchronize(v[i + 1]) != cudaSuccess)
+            return set_status(ctx, FVIF_ECUDA);
+        float t = 0.0f;
+        if (cudaEventElapsedTime(&t, v[i], v[i + 1]) != cudaSuccess)
+            return set_status(ctx, FVIF_ECUDA);
+        ms += t;
+    }
+    *total_ms = ms;
+    *launches = ctx->launches[kind];
+    return set_status(ctx, FVIF_OK);
+}
+
+int fvif_chunk_frames(const fvif_ctx *ctx)
+{
+    return ctx ? ctx->chunk : FVIF_EINVAL;
+}
+
+int fvif_get_taps(const fvif_ctx *ctx, int scale, float *taps, int cap)
+{
+    if (!ctx || !taps || scale < 0 || scale >= kScales)
+        return FVIF_EINVAL;
+    const Taps &t = ctx->taps[scale];
+    if (cap < t.n)
+        return FVIF_EINVAL;
+    std::memcpy(taps, t.t, sizeof(float) * t.n);
+    return t.n;
+}
+
+int fvif_score_async(fvif_ctx *ctx, const void *ref, const void *dist,
+                     int n_frames, double *out)
+{
+    if (!ctx)
+        return FVIF_EINVAL;
+    if (n_frames < 0 || (n_frames > 0 && (!ref || !dist || !out)))
+        return set_status(ctx, FVIF_EINVAL);
+    if (n_frames == 0)
+        return set_status(ctx, FVIF_OK);
+    DeviceGuard g(ctx->device);
+    if (!g.ok)
+        return set_status(ctx, FVIF_ECUDA);
+    return set_status(ctx, enqueue_all(ctx, ref, dist, n_frames, out));
+}
+
+int fvif_score(fvif_ctx *ctx, const void *ref, const void *dist, int n_frames,
+               double *out)
+{
+    if (!ctx)
+        return FVIF_EINVAL;
+    if (n_frames < 0 || (n_frames > 0 && (!ref || !dist || !out)))
+        return set_status(ctx, FVIF_EINVAL);
+    if (n_frames == 0)
+        return set_status(ctx, FVIF_OK);
+    DeviceGuard g(ctx->device);
+    if (!g.ok)
+        return set_status(ctx, FVIF_ECUDA);
+    int st = ensure_out(ctx, n_frames);
+    if (st == FVIF_OK)
+        st = enqueue_all(ctx, ref, dist, n_frames, ctx->d_out);
+    if (st == FVIF_OK)
+        st = finish_to_host(ctx, n_frames, out);
+    return set_status(ctx, st);
+}
+
+int fvif_score_host(fvif_ctx *ctx, const void *ref, const void *dist,
+                    int n_frames, double *out)
+{
+    if (!ctx)
+        return FVIF_EINVAL;
+    if (n_frames < 0 || (n_frames > 0 && (!ref || !dist || !out)))
+        return set_status(ctx, FVIF_EINVAL);
+    if (n_frames == 0)
+        return set_status(ctx, FVIF_OK);
+    DeviceGuard g(ctx->device);
+    if (!g.ok)
+        return set_status(ctx, FVIF_ECUDA);
+    int st = ensure_out(ctx, n_frames);
+    if (st == FVIF_OK)
+        st = ensure_pipeline(ctx);
+    if (st != FVIF_OK)
+        return set_status(ctx, st);
+
+    const size_t fb = ctx->frame_bytes();
+    const size_t half = fb * (size_t)ctx->chunk;
+    cudaError_t e = cudaSuccess;
+    int i = 0;
+    for (int f0 = 0; f0 < n_frames && e == cudaSuccess; f0 += ctx->chunk, ++i) {
+        const int nf = (n_frames - f0 < ctx->chunk) ? n_frames - f0
+                                                    : ctx->chunk;
+        const int slot = i & 1;
+        unsigned char *dref = ctx->stage[slot];
+        unsigned char *ddist = ctx->stage[slot] + half;
+        /* the slot is free once the chunk that used it two steps ago ran */
+        e = cudaStreamWaitEvent(ctx->copy_stream, ctx->consumed[slot], 0);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(dref,
+                                static_cast<const unsigned char *>(ref) +
+                                    fb * f0,
+                                fb * nf, cudaMemcpyHostToDevice,
+                                ctx->copy_stream);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(ddist,
+                                static_cast<const unsigned char *>(dist) +
+                                    fb * f0,
+                                fb * nf, cudaMemcpyHostToDevice,
+                                ctx->copy_stream);
+        if (e == cudaSuccess)
+            e = cudaEventRecord(ctx->copied[slot], ctx->copy_stream);
+        if (e == cudaSuccess)
+            e = cudaStreamWaitEvent(ctx->stream, ctx->copied[slot], 0);
+        if (e != cudaSuccess)
+            break;
+        st = run_chunk(ctx, dref, ddist, nf,
+                       ctx->d_out + (size_t)kScales * f0, nullptr);
+        if (st != FVIF_OK)
+            return set_status(ctx, st);
+        e = cudaEventRecord(ctx->consumed[slot], ctx->stream);
+    }
+    if (e != cudaSuccess) {
+        cudaStreamSynchronize(ctx->copy_stream);
+        return set_status(ctx, cuda_status(e));
+    }
+    return set_status(ctx, finish_to_host(ctx, n_frames, out));
+}
+
+int fvif_debug_frame(fvif_ctx *ctx, const void *ref, const void *dist,
+                     float *planes, float *rows, float *sums)
+{
+    if (!ctx)
+        return FVIF_EINVAL;
+    if (!ref || !dist)
+        return set_status(ctx, FVIF_EINVAL);
+    DeviceGuard g(ctx->device);
+    if (!g.ok)
+        return set_status(ctx, FVIF_ECUDA);
+    const int st = run_chunk(ctx, ref, dist, 1, ctx->d_out, ctx->sums);
+    if (st != FVIF_OK)
+        return set_status(ctx, st);
+    cudaError_t e = cudaSuccess;
+    if (planes) {
+        size_t total = 0;
+        for (int s = 0; s < kScales; ++s)
+            total += 2 * (size_t)ctx->ws[s] * ctx->hs[s];
+        float *tmp = nullptr;
+        e = cudaMalloc(&tmp, sizeof(float) * total);
+        size_t off = 0;
+        for (int s = 0; s < kScales && e == cudaSuccess; ++s) {
+            const size_t np = (size_t)ctx->ws[s] * ctx->hs[s];
+            const SrcDesc d = s == 0 ? scale0_src(ctx, ref, dist)
+                                     : pyr_src(ctx, s);
+            e = launch_unpack_planes(d, ctx->ws[s], ctx->hs[s], tmp + off,
+                                     tmp + off + np, ctx->stream);
+            off += 2 * np;
+        }
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(planes, tmp, sizeof(float) * total,
+                                cudaMemcpyDeviceToHost, ctx->stream);
+        if (e == cudaSuccess)
+            e = cudaStreamSynchronize(ctx->stream);
+        if (tmp)
+            cudaFree(tmp);
+        if (e != cudaSuccess)
+            return set_status(ctx, cuda_status(e));
+    }
+    if (rows) {
+        size_t off = 0;
+        for (int s = 0; s < kScales && e == cudaSuccess; ++s) {
+            e = cudaMemcpyAsync(rows + off, ctx->rows + ctx->rows_base[s],
+                                sizeof(float2) * ctx->hs[s],
+                                cudaMemcpyDeviceToHost, ctx->stream);
+            off += 2 * (size_t)ctx->hs[s];
+        }
+    }
+    if (sums && e == cudaSuccess)
+        e = cudaMemcpyAsync(sums, ctx->sums, sizeof(float2) * kScales,
+                            cudaMemcpyDeviceToHost, ctx->stream);
+    if (e == cudaSuccess)
+        e = cudaStreamSynchronize(ctx->stream);
+    return set_status(ctx, cuda_status(e));
+}
+
+} // extern "C"

@@ -1,0 +1,144 @@
+/* Decimation kernels, the per-(frame, scale) final reduction and the plane
+ * unpacking used by the diagnostics entry point. */
+#include "fvif_dispatch.cuh"
+
+namespace fvif {
+
+cudaError_t stats_dispatch_u8(const StatsArgs &, const Taps &, cudaStream_t);
+cudaError_t stats_dispatch_u16(const StatsArgs &, const Taps &, cudaStream_t);
+cudaError_t stats_dispatch_f2(const StatsArgs &, const Taps &, cudaStream_t);
+
+static const int kSpecU[] = {5, 9, 19};
+static const int kSpecF2[] = {1, 3, 5, 7, 11};
+static const int kSpecStats[] = {1, 3, 5, 7, 9, 11, 17, 19, 35};
+
+bool stats_is_specialised(int ntaps)
+{
+    for (int n : kSpecStats)
+        if (n == ntaps)
+            return true;
+    return false;
+}
+
+bool decimate_is_specialised(int ntaps)
+{
+    for (int n : kSpecU)
+        if (n == ntaps)
+            return true;
+    for (int n : kSpecF2)
+        if (n == ntaps)
+            return true;
+    return false;
+}
+
+cudaError_t launch_stats(const StatsArgs &a, const Taps &tp, cudaStream_t st)
+{
+    switch (a.src.kind) {
+    case SrcKind::U8: return stats_dispatch_u8(a, tp, st);
+    case SrcKind::U16: return stats_dispatch_u16(a, tp, st);
+    default: return stats_dispatch_f2(a, tp, st);
+    }
+}
+
+template <SrcKind K>
+static cudaError_t dec_dispatch_u(const DecArgs &a, const Taps &tp,
+                                  cudaStream_t st)
+{
+    switch (tp.n) {
+    case 5: return run_decimate<5, K>(a, tp, st);
+    case 9: return run_decimate<9, K>(a, tp, st);
+    case 19: return run_decimate<19, K>(a, tp, st);
+    default: return run_decimate<0, K>(a, tp, st);
+    }
+}
+
+cudaError_t launch_decimate(const DecArgs &a, const Taps &tp, cudaStream_t st)
+{
+    switch (a.src.kind) {
+    case SrcKind::U8: return dec_dispatch_u<SrcKind::U8>(a, tp, st);
+    case SrcKind::U16: return dec_dispatch_u<SrcKind::U16>(a, tp, st);
+    default:
+        switch (tp.n) {
+        case 1: return run_decimate<1, SrcKind::F2>(a, tp, st);
+        case 3: return run_decimate<3, SrcKind::F2>(a, tp, st);
+        case 5: return run_decimate<5, SrcKind::F2>(a, tp, st);
+        case 7: return run_decimate<7, SrcKind::F2>(a, tp, st);
+        case 11: return run_decimate<11, SrcKind::F2>(a, tp, st);
+        default: return run_decimate<0, SrcKind::F2>(a, tp, st);
+        }
+    }
+}
+
+/* One warp per (frame, scale): the row sums added top to bottom into one
+ * fp32 accumulator per output, then vif_scale = num / den in fp64
+ * ("ADR-1422 ...", Decision: the rows' sums are added top to bottom in
+ * fp32).  Every lane carries the same running sums; lane 0 writes. */
+__global__ void final_kernel(const FinalArgs a)
+{
+    const int warp = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+    const int lane = threadIdx.x & 31;
+    if (warp >= a.nframes * kScales)
+        return;
+    const int f = warp / kScales, s = warp % kScales;
+    const int h = a.h[s];
+    const float2 *r = a.rows + (size_t)f * a.rows_stride + a.rows_base[s];
+    float num = 0.0f, den = 0.0f;
+    for (int b = 0; b < h; b += 32) {
+        const float2 v = (b + lane < h) ? r[b + lane] : make_float2(0.f, 0.f);
+        const int cnt = min(32, h - b);
+        for (int j = 0; j < cnt; ++j) {
+            num = __fadd_rn(num, __shfl_sync(0xffffffffu, v.x, j));
+            den = __fadd_rn(den, __shfl_sync(0xffffffffu, v.y, j));
+        }
+    }
+    if (lane == 0) {
+        a.out[(size_t)f * kScales + s] = __ddiv_rn((double)num, (double)den);
+        if (a.sums)
+            a.sums[(size_t)f * kScales + s] = make_float2(num, den);
+    }
+}
+
+cudaError_t launch_final(const FinalArgs &a, cudaStream_t st)
+{
+    const int warps = a.nframes * kScales;
+    const int threads = 128;
+    const int blocks = (warps * 32 + threads - 1) / threads;
+    final_kernel<<<blocks, threads, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+template <SrcKind K>
+__global__ void unpack_kernel(const SrcDesc d, int n, float *xo, float *yo)
+{
+    const Plane<K> p(d, 0);
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n;
+         i += gridDim.x * blockDim.x) {
+        const float2 v = p.at(i, d.scale);
+        xo[i] = v.x;
+        yo[i] = v.y;
+    }
+}
+
+cudaError_t launch_unpack_planes(const SrcDesc &src, int w, int h,
+                                 float *ref_out, float *dist_out,
+                                 cudaStream_t st)
+{
+    const int n = w * h;
+    const int blocks = (n + 255) / 256;
+    switch (src.kind) {
+    case SrcKind::U8:
+        unpack_kernel<SrcKind::U8><<<blocks, 256, 0, st>>>(src, n, ref_out,
+                                                           dist_out);
+        break;
+    case SrcKind::U16:
+        unpack_kernel<SrcKind::U16><<<blocks, 256, 0, st>>>(src, n, ref_out,
+                                                            dist_out);
+        break;
+    default:
+        unpack_kernel<SrcKind::F2><<<blocks, 256, 0, st>>>(src, n, ref_out,
+                                                           dist_out);
+    }
+    return cudaGetLastError();
+}
+
+} // namespace fvif

@@ -1,0 +1,80 @@
+/*
+ * fvif_internal.h -- declarations shared by the library's translation units
+ * (host API and kernel instantiations).  Not part of the public ABI.
+ */
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace fvif {
+
+constexpr int kScales = 4;
+constexpr int kMaxRadius = 64;               /* largest half-width accepted  */
+constexpr int kMaxTaps = 2 * kMaxRadius + 1; /* 129                          */
+
+/* Taps of one scale, handed to a launch by value (kernel parameter space),
+ * so compile-time-indexed reads become constant-bank operands.            */
+struct Taps {
+    float t[kMaxTaps];
+    int n;
+};
+
+/* Where the samples of one plane come from. */
+enum class SrcKind { U8, U16, F2 };
+
+struct SrcDesc {
+    SrcKind kind;
+    const void *x;     /* U8/U16: ref samples; F2: interleaved (ref, dist)  */
+    const void *y;     /* U8/U16: dist samples; F2: unused                  */
+    float scale;       /* U16: 2^-(bitdepth-8); otherwise 1                 */
+    size_t frame_elems;/* samples per frame of this plane                   */
+};
+
+/* Per-scale statistic launch: all frames of a chunk, one CTA per strip. */
+struct StatsArgs {
+    SrcDesc src;
+    int w, h;          /* plane size at this scale                          */
+    int nframes;
+    double nsq;
+    float gain_limit;
+    float2 *rows;      /* row sums, (num, den)                              */
+    int rows_stride;   /* float2 per frame in rows                          */
+    int rows_base;     /* offset of this scale inside a frame's rows        */
+};
+
+/* Decimation launch: plane s (w x h) -> plane s+1 (w/2 x h/2), float2. */
+struct DecArgs {
+    SrcDesc src;
+    int w, h;
+    int nframes;
+    float2 *dst;
+    size_t dst_frame_elems;
+};
+
+/* Final per-(frame, scale) reduction over the row sums. */
+struct FinalArgs {
+    const float2 *rows;
+    int rows_stride;
+    int rows_base[kScales];
+    int h[kScales];
+    int nframes;
+    double *out;       /* device, 4 per frame                               */
+    float2 *sums;      /* optional device (num, den) per (frame, scale)     */
+};
+
+cudaError_t launch_stats(const StatsArgs &a, const Taps &taps,
+                         cudaStream_t st);
+cudaError_t launch_decimate(const DecArgs &a, const Taps &taps,
+                            cudaStream_t st);
+cudaError_t launch_final(const FinalArgs &a, cudaStream_t st);
+cudaError_t launch_unpack_planes(const SrcDesc &src, int w, int h,
+                                 float *ref_out, float *dist_out,
+                                 cudaStream_t st);
+
+/* Tap widths that have a specialised (fully unrolled) kernel. */
+bool stats_is_specialised(int ntaps);
+bool decimate_is_specialised(int ntaps);
+
+} // namespace fvif

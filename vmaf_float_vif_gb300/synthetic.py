@@ -12,6 +12,8 @@ and on ``f`` (numpy ``default_rng`` seeded per frame).  Samples are uint8 for
 """
 from __future__ import annotations
 
+import os
+from concurrent.futures import ThreadPoolExecutor
 from dataclasses import dataclass, field
 from typing import Callable, Dict, List, Sequence, Tuple
 
@@ -44,8 +46,18 @@ class Case:
         return ref.astype(self.dtype), dist.astype(self.dtype)
 
     def batch(self, idx: Sequence[int]) -> Tuple[np.ndarray, np.ndarray]:
-        refs, dists = zip(*(self.pair(f) for f in idx))
+        refs, dists = zip(*_parallel_pairs(self, list(idx)))
         return np.stack(refs), np.stack(dists)
+
+
+def _parallel_pairs(case: "Case", idx: List[int]):
+    """Generate several pairs on host threads (numpy's FFT and array code
+    release the GIL); results are identical to one-by-one generation."""
+    if len(idx) <= 1 or case.w * case.h < 1 << 18:
+        return [case.pair(f) for f in idx]
+    workers = max(1, min(len(idx), os.cpu_count() or 1))
+    with ThreadPoolExecutor(max_workers=workers) as ex:
+        return list(ex.map(case.pair, idx))
 
 
 def _round_half_up(a: np.ndarray) -> np.ndarray:
@@ -195,3 +207,25 @@ def custom_noise_case(w: int, h: int, bitdepth: int, frames: int = 1,
                 np.clip(d * scale + lo, 0, top))
     return Case("noise_%dx%d_%db" % (w, h, bitdepth), w, h, bitdepth, frames,
                 make)
+
+
+def streamed_batch(case: Case, n_frames: int, distinct: int = 16,
+                   start: int = 0) -> Tuple[np.ndarray, np.ndarray]:
+    """n_frames pairs built from ``distinct`` generated pairs: frame f is pair
+    (f mod distinct) circularly shifted by 37 * (f // distinct) px in x and
+    y (both planes alike), so every frame of a long stream differs while
+    generation stays cheap.  Used for the 240-frame 4K stream."""
+    keys = sorted(set((start + i) % distinct for i in range(n_frames)))
+    base = dict(zip(keys, _parallel_pairs(case, keys)))
+    refs = np.empty((n_frames, case.h, case.w), case.dtype)
+    dists = np.empty_like(refs)
+    for i in range(n_frames):
+        f = start + i
+        r, d = base[f % distinct]
+        sh = 37 * (f // distinct)
+        if sh:
+            r = np.roll(r, (sh, sh), axis=(0, 1))
+            d = np.roll(d, (sh, sh), axis=(0, 1))
+        refs[i] = r
+        dists[i] = d
+    return refs, dists
