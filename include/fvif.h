@@ -45,7 +45,8 @@ enum fvif_status {
     FVIF_OK = 0,
     FVIF_EINVAL = -1, /* invalid argument (size, bit depth, pointer, ...) */
     FVIF_ENOMEM = -2, /* device or pinned host allocation failed */
-    FVIF_ECUDA = -3   /* a CUDA call or kernel launch failed */
+    FVIF_ECUDA = -3,  /* a CUDA call or kernel launch failed */
+    FVIF_ETOOBIG = -4 /* frame too large for fvif_score_noalloc's scratch */
 };
 
 /* Create a context for frames of w x h samples.
@@ -138,6 +139,44 @@ int fvif_profile_enable(fvif_ctx *ctx, int enable);
  * Launch counts are kept even when timing is disabled. */
 int fvif_profile_read(fvif_ctx *ctx, int kind, double *total_ms,
                       long long *launches);
+
+/* Size in bytes of the fixed device scratch array used by
+ * fvif_score_noalloc (8 MiB). */
+#define FVIF_NOALLOC_SCRATCH_BYTES (8u * 1024u * 1024u)
+
+/* Score frame pairs without allocating anything (no counterpart in the
+ * pages: it exists for callers of this library that may not call cudaMalloc
+ * -- code under a device memory arena or caching allocator that must own
+ * every allocation, real-time loops that cannot take cudaMalloc's implicit
+ * synchronisation, plug-ins with a fixed device-memory budget).
+ *
+ * Same arguments and results as fvif_create followed by fvif_score_async,
+ * with no context: ref, dist (n_frames frames) and out (4*n_frames doubles)
+ * are DEVICE memory owned by the caller; work is enqueued on cuda_stream
+ * (NULL = legacy default stream) and the call returns without waiting.
+ * Frames are scored one at a time through the same kernels as fvif_score,
+ * with the intermediate planes and row sums kept in one file-scope device
+ * array of FVIF_NOALLOC_SCRATCH_BYTES that the library holds on every GPU
+ * where it is loaded, until the process exits.
+ *
+ * Limit: a frame needs, rounding each part up to 256 bytes,
+ * 8*(w1*h1) + 8*(w2*h2) + 8*(w3*h3) + 8*(h0+h1+h2+h3) bytes, where
+ * w_s = w >> s and h_s = h >> s; frames whose need exceeds the array are
+ * rejected with FVIF_ETOOBIG before anything is launched (1920x1080 needs
+ * about 5.5 MB and fits; 3840x2160 does not).
+ *
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  Every call uses the same array and leaves its
+ * last contents there; nothing in it needs to start at zero.  Calls whose
+ * work overlaps on the GPU (different streams, or several host threads)
+ * race on the array: serialise them, e.g. on one stream.
+ *
+ * Returns FVIF_OK, FVIF_EINVAL (argument outside the ranges of
+ * fvif_create, NULL buffer, negative count), FVIF_ETOOBIG or FVIF_ECUDA. */
+int fvif_score_noalloc(int w, int h, int bitdepth, float kernelscale,
+                       double sigma_nsq, const void *ref, const void *dist,
+                       int n_frames, double *out, void *cuda_stream);
 
 #ifdef __cplusplus
 }

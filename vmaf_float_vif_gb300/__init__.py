@@ -11,7 +11,8 @@ PyTorch is used only as a source of device memory and streams (tensors'
 serve as host buffers.
 """
 from ._lib import (  # noqa: F401
-    FVIF_EINVAL, FVIF_ENOMEM, FVIF_ECUDA, FVIF_OK, FvifError, build, lib,
+    FVIF_EINVAL, FVIF_ENOMEM, FVIF_ECUDA, FVIF_ETOOBIG, FVIF_OK, FvifError,
+    NOALLOC_SCRATCH_BYTES, build, lib, fvif_score_noalloc,
     fvif_chunk_frames, fvif_create, fvif_debug_frame, fvif_destroy,
     fvif_get_taps, fvif_last_error, fvif_score, fvif_score_async,
     fvif_score_host, fvif_set_stream, fvif_strerror, fvif_profile_enable,

@@ -18,7 +18,7 @@ OUT_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(OUT_DIR, "libfvif.so")
 
 SOURCES = ["fvif_api.cu", "fvif_stats_u8.cu", "fvif_stats_u16.cu",
-           "fvif_stats_f2.cu", "fvif_decimate.cu"]
+           "fvif_stats_f2.cu", "fvif_decimate.cu", "fvif_noalloc.cu"]
 HEADERS = ["fvif_internal.h", "fvif_kernels.cuh", "fvif_dispatch.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

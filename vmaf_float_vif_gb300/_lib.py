@@ -19,13 +19,15 @@ FVIF_OK = 0
 FVIF_EINVAL = -1
 FVIF_ENOMEM = -2
 FVIF_ECUDA = -3
+FVIF_ETOOBIG = -4
+NOALLOC_SCRATCH_BYTES = 8 * 1024 * 1024
 
 # Every symbol include/fvif.h declares.
 EXPORTS = (
     "fvif_create", "fvif_score", "fvif_score_async", "fvif_score_host",
     "fvif_destroy", "fvif_set_stream", "fvif_last_error", "fvif_strerror",
     "fvif_chunk_frames", "fvif_get_taps", "fvif_debug_frame",
-    "fvif_profile_enable", "fvif_profile_read",
+    "fvif_profile_enable", "fvif_profile_read", "fvif_score_noalloc",
 )
 
 FVIF_K_DECIMATE, FVIF_K_STATS0, FVIF_K_STATS123, FVIF_K_FINAL = range(4)
@@ -48,7 +50,8 @@ def _strerror_safe(status: int) -> str:
         return lib().fvif_strerror(status).decode()
     except Exception:  # library itself unavailable
         return {0: "ok", -1: "invalid argument", -2: "out of memory",
-                -3: "CUDA error"}.get(status, "unknown status")
+                -3: "CUDA error", -4: "frame too large"}.get(
+                    status, "unknown status")
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
@@ -83,6 +86,8 @@ def _declare(L: ctypes.CDLL) -> ctypes.CDLL:
     L.fvif_profile_enable.restype = i
     L.fvif_profile_read.argtypes = [vp, i, dp, ctypes.POINTER(ctypes.c_longlong)]
     L.fvif_profile_read.restype = i
+    L.fvif_score_noalloc.argtypes = [i, i, i, f, d, vp, vp, i, vp, vp]
+    L.fvif_score_noalloc.restype = i
     return L
 
 
@@ -270,6 +275,33 @@ def fvif_debug_frame(ctx: int, ref, dist, w: int, h: int, bitdepth: int):
         out["rows"].append(rows[ro:ro + 2 * hs].reshape(hs, 2))
         ro += 2 * hs
     return out
+
+
+def fvif_score_noalloc(ref, dist, out, w: int, h: int, bitdepth: int,
+                       kernelscale: float = 1.0, sigma_nsq: float = 2.0,
+                       stream=None) -> None:
+    """Score device frames into a device float64 ``out`` (4 per frame)
+    without any allocation by the library: for callers that may not call
+    cudaMalloc (memory arenas, real-time loops).  Enqueues on ``stream``
+    and returns; intermediates live in the library's fixed 8 MiB device
+    array, so calls that overlap on the GPU must be serialised."""
+    import torch
+    n = _frames(ref, w, h)
+    if _frames(dist, w, h) != n:
+        raise ValueError("ref and dist hold different frame counts")
+    if (not isinstance(out, torch.Tensor) or not out.is_cuda or
+            out.dtype != torch.float64 or out.numel() < 4 * n or
+            not out.is_contiguous()):
+        raise TypeError("out must be a contiguous CUDA float64 tensor of "
+                        ">= 4*n values")
+    handle = getattr(stream, "cuda_stream", stream)
+    st = lib().fvif_score_noalloc(int(w), int(h), int(bitdepth),
+                                  float(kernelscale), float(sigma_nsq),
+                                  _dev_ptr(ref, bitdepth, "ref"),
+                                  _dev_ptr(dist, bitdepth, "dist"), n,
+                                  out.data_ptr(), handle or None)
+    if st:
+        raise FvifError(st, "fvif_score_noalloc")
 
 
 def fvif_profile_enable(ctx: int, enable: bool) -> None:

@@ -20,6 +20,10 @@ constexpr int kDefaultChunk = 16;
 
 thread_local int g_create_status = FVIF_OK;
 
+} // namespace
+
+namespace fvif {
+
 /* Taps of scale s for kernelscale ks.  "ADR-1422: float_vif_sycl computes
  * the CPU's arithmetic without an fp64 type ...", Decision: the taps are the
  * CPU routine's, computed at run time for (float)vif_kernelscale and handed
@@ -54,6 +58,10 @@ int make_taps(float kernelscale, int s, Taps &out)
         out.t[k] = (float)(wk[k] / sum);
     return FVIF_OK;
 }
+
+} // namespace fvif
+
+namespace {
 
 /* Keeps the caller's current device; switches to the context's for the
  * duration of one API call. */
@@ -444,6 +452,8 @@ const char *fvif_strerror(int status)
     case FVIF_EINVAL: return "invalid argument";
     case FVIF_ENOMEM: return "out of memory";
     case FVIF_ECUDA: return "CUDA error";
+    case FVIF_ETOOBIG:
+        return "frame too large for the no-allocation entry point's scratch";
     default: return "unknown status";
     }
 }

@@ -64,6 +64,9 @@ struct FinalArgs {
     float2 *sums;      /* optional device (num, den) per (frame, scale)     */
 };
 
+/* Taps of scale s for a kernelscale (host); FVIF_OK or FVIF_EINVAL. */
+int make_taps(float kernelscale, int s, Taps &out);
+
 cudaError_t launch_stats(const StatsArgs &a, const Taps &taps,
                          cudaStream_t st);
 cudaError_t launch_decimate(const DecArgs &a, const Taps &taps,
