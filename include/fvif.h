@@ -120,6 +120,17 @@ int fvif_get_taps(const fvif_ctx *ctx, int scale, float *taps, int cap);
 int fvif_debug_frame(fvif_ctx *ctx, const void *ref, const void *dist,
                      float *planes, float *rows, float *sums);
 
+/* The per-pixel statistic and terms of the context's kernels applied to n
+ * given filtered statistics (mu1, mu2, xx, yy, xy; all DEVICE arrays of n
+ * floats): num[i], den[i] receive the two log terms.  fallbacks (DEVICE,
+ * may be NULL) is incremented once per pixel whose terms needed the native
+ * fp64 sequence.  Enqueued on the context stream.  Diagnostics: checks the
+ * term evaluation on arbitrary inputs. */
+int fvif_debug_terms(fvif_ctx *ctx, const float *mu1, const float *mu2,
+                     const float *xx, const float *yy, const float *xy,
+                     int n, float *num, float *den,
+                     unsigned long long *fallbacks);
+
 /* Kernel kinds for the profiling counters. */
 enum fvif_kernel_kind {
     FVIF_K_DECIMATE = 0, /* the three decimation launches of a chunk      */

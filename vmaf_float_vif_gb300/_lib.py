@@ -28,6 +28,7 @@ EXPORTS = (
     "fvif_destroy", "fvif_set_stream", "fvif_last_error", "fvif_strerror",
     "fvif_chunk_frames", "fvif_get_taps", "fvif_debug_frame",
     "fvif_profile_enable", "fvif_profile_read", "fvif_score_noalloc",
+    "fvif_debug_terms",
 )
 
 FVIF_K_DECIMATE, FVIF_K_STATS0, FVIF_K_STATS123, FVIF_K_FINAL = range(4)
@@ -86,6 +87,8 @@ def _declare(L: ctypes.CDLL) -> ctypes.CDLL:
     L.fvif_profile_enable.restype = i
     L.fvif_profile_read.argtypes = [vp, i, dp, ctypes.POINTER(ctypes.c_longlong)]
     L.fvif_profile_read.restype = i
+    L.fvif_debug_terms.argtypes = [vp] + [vp] * 5 + [i, vp, vp, vp]
+    L.fvif_debug_terms.restype = i
     L.fvif_score_noalloc.argtypes = [i, i, i, f, d, vp, vp, i, vp, vp]
     L.fvif_score_noalloc.restype = i
     return L
@@ -321,6 +324,28 @@ def fvif_profile_read(ctx: int, kind: int):
     return ms.value, n.value
 
 
+def fvif_debug_terms(ctx: int, mu1, mu2, xx, yy, xy, count_fallbacks=True):
+    """Per-pixel terms of device float32 tensors -> (num, den, fallbacks)."""
+    import torch
+    ts = [mu1, mu2, xx, yy, xy]
+    n = ts[0].numel()
+    for t in ts:
+        if (not isinstance(t, torch.Tensor) or not t.is_cuda or
+                t.dtype != torch.float32 or t.numel() != n or
+                not t.is_contiguous()):
+            raise TypeError("statistics must be contiguous CUDA float32 "
+                            "tensors of one length")
+    num = torch.empty(n, dtype=torch.float32, device=ts[0].device)
+    den = torch.empty_like(num)
+    fb = torch.zeros(1, dtype=torch.int64, device=ts[0].device)
+    st = lib().fvif_debug_terms(ctx, *[t.data_ptr() for t in ts], n,
+                                num.data_ptr(), den.data_ptr(),
+                                fb.data_ptr() if count_fallbacks else None)
+    if st:
+        raise FvifError(st, "fvif_debug_terms")
+    return num, den, fb
+
+
 class Context:
     """Owning wrapper: ``with Context(w, h, bd, ks, nsq) as c: c.score(...)``."""
 
@@ -364,6 +389,10 @@ class Context:
 
     def taps(self, scale: int) -> np.ndarray:
         return fvif_get_taps(self.handle, scale)
+
+    def debug_terms(self, mu1, mu2, xx, yy, xy, count_fallbacks=True):
+        return fvif_debug_terms(self.handle, mu1, mu2, xx, yy, xy,
+                                count_fallbacks)
 
     def debug_frame(self, ref, dist):
         return fvif_debug_frame(self.handle, ref, dist, self.w, self.h,

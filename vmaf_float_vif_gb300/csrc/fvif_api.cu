@@ -59,6 +59,32 @@ int make_taps(float kernelscale, int s, Taps &out)
     return FVIF_OK;
 }
 
+/* Constants of the per-pixel statistic.  nsq_up makes the fp64 comparison
+ * (double)s1 < nsq an fp32 one: for an fp32 s1, s1 < nsq exactly when s1 is
+ * below the smallest fp32 value not below nsq.  n_hi + n_lo carries nsq to
+ * 2^-48 for the pair evaluation, which is used only for nsq in
+ * [2^-60, 2^60] so that every pair quantity stays a normal fp32 value.    */
+void make_term_params(double nsq, float gain_limit, int mode, TermParams &t)
+{
+    std::memset(&t, 0, sizeof t);
+    t.nsq = nsq;
+    t.gain_limit = gain_limit;
+    float up = (float)nsq;
+    if ((double)up < nsq)
+        up = std::nextafter(up, INFINITY);
+    t.nsq_up = up;
+    const bool in_range = nsq >= 0x1p-60 && nsq <= 0x1p60;
+    t.mode = in_range ? mode : kTermsFp64;
+    if (in_range) {
+        t.n_hi = (float)nsq;
+        t.n_lo = (float)(nsq - (double)t.n_hi);
+        t.rcp_n = (float)(1.0 / (double)t.n_hi);
+        int e = 0;
+        const double m = std::frexp(nsq, &e); /* nsq = m 2^e, m in [0.5, 1) */
+        t.inv_pow2 = (m == 0.5) ? (float)std::ldexp(1.0, 1 - e) : 0.0f;
+    }
+}
+
 } // namespace fvif
 
 namespace {
@@ -89,6 +115,7 @@ struct fvif_ctx {
     float kernelscale = 1.0f;
     double nsq = 2.0;
     float gain_limit = 100.0f;
+    TermParams terms;
     int ws[kScales] = {}, hs[kScales] = {};
     Taps taps[kScales];
     int chunk = kDefaultChunk;
@@ -249,8 +276,7 @@ int run_chunk(fvif_ctx *c, const void *ref, const void *dist, int nf,
         a.w = c->ws[s];
         a.h = c->hs[s];
         a.nframes = nf;
-        a.nsq = c->nsq;
-        a.gain_limit = c->gain_limit;
+        a.terms = c->terms;
         a.rows = c->rows;
         a.rows_stride = c->rows_stride;
         a.rows_base = c->rows_base[s];
@@ -381,6 +407,12 @@ fvif_ctx *fvif_create(int w, int h, int bitdepth, float kernelscale,
     c->bitdepth = bitdepth;
     c->kernelscale = kernelscale;
     c->nsq = sigma_nsq;
+    {
+        const char *mode = std::getenv("FVIF_TERMS");
+        const int m = (mode && std::strcmp(mode, "fp64") == 0) ? kTermsFp64
+                                                               : kTermsPair;
+        make_term_params(sigma_nsq, c->gain_limit, m, c->terms);
+    }
     for (int s = 0; s < kScales; ++s) {
         c->ws[s] = s == 0 ? w : c->ws[s - 1] / 2;
         c->hs[s] = s == 0 ? h : c->hs[s - 1] / 2;
@@ -604,6 +636,26 @@ int fvif_score_host(fvif_ctx *ctx, const void *ref, const void *dist,
         return set_status(ctx, cuda_status(e));
     }
     return set_status(ctx, finish_to_host(ctx, n_frames, out));
+}
+
+int fvif_debug_terms(fvif_ctx *ctx, const float *mu1, const float *mu2,
+                     const float *xx, const float *yy, const float *xy,
+                     int n, float *num, float *den,
+                     unsigned long long *fallbacks)
+{
+    if (!ctx)
+        return FVIF_EINVAL;
+    if (n < 0 || (n > 0 && (!mu1 || !mu2 || !xx || !yy || !xy || !num ||
+                            !den)))
+        return set_status(ctx, FVIF_EINVAL);
+    if (n == 0)
+        return set_status(ctx, FVIF_OK);
+    DeviceGuard g(ctx->device);
+    if (!g.ok)
+        return set_status(ctx, FVIF_ECUDA);
+    return set_status(ctx, cuda_status(launch_terms(ctx->terms, mu1, mu2, xx,
+                                                    yy, xy, n, num, den,
+                                                    fallbacks, ctx->stream)));
 }
 
 int fvif_debug_frame(fvif_ctx *ctx, const void *ref, const void *dist,

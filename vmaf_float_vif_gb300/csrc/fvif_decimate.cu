@@ -107,6 +107,40 @@ cudaError_t launch_final(const FinalArgs &a, cudaStream_t st)
     return cudaGetLastError();
 }
 
+__global__ void terms_kernel(const TermParams tp, const float *mu1,
+                             const float *mu2, const float *xx,
+                             const float *yy, const float *xy, int n,
+                             float *num, float *den,
+                             unsigned long long *fallbacks)
+{
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n;
+         i += gridDim.x * blockDim.x) {
+        float a, b;
+        if (fallbacks)
+            pixel_terms<true>(mu1[i], mu2[i], xx[i], yy[i], xy[i], tp, a, b,
+                              fallbacks);
+        else
+            pixel_terms<false>(mu1[i], mu2[i], xx[i], yy[i], xy[i], tp, a, b,
+                               nullptr);
+        num[i] = a;
+        den[i] = b;
+    }
+}
+
+cudaError_t launch_terms(const TermParams &tp, const float *mu1,
+                         const float *mu2, const float *xx, const float *yy,
+                         const float *xy, int n, float *num, float *den,
+                         unsigned long long *fallbacks, cudaStream_t st)
+{
+    const int threads = 256;
+    int blocks = (n + threads - 1) / threads;
+    if (blocks > 152 * 32)
+        blocks = 152 * 32;
+    terms_kernel<<<blocks, threads, 0, st>>>(tp, mu1, mu2, xx, yy, xy, n, num,
+                                             den, fallbacks);
+    return cudaGetLastError();
+}
+
 template <SrcKind K>
 __global__ void unpack_kernel(const SrcDesc d, int n, float *xo, float *yo)
 {

@@ -32,13 +32,30 @@ struct SrcDesc {
     size_t frame_elems;/* samples per frame of this plane                   */
 };
 
+/* How the two fp64 terms are evaluated. */
+enum TermsMode {
+    kTermsPair = 0, /* fp32 pairs, native fp64 only where undecided */
+    kTermsFp64 = 1  /* native fp64 on every log-branch pixel        */
+};
+
+/* Constants of the per-pixel statistic, derived once on the host from the
+ * fp64 noise variance (make_term_params). */
+struct TermParams {
+    double nsq;       /* vif_sigma_nsq                                      */
+    float gain_limit;
+    float nsq_up;     /* smallest fp32 >= nsq: (double)s < nsq <=> s < nsq_up */
+    float n_hi, n_lo; /* nsq = n_hi + n_lo + e, |e| <= 2^-48 nsq            */
+    float rcp_n;      /* fl32(1 / n_hi)                                     */
+    float inv_pow2;   /* 1 / nsq when nsq is a power of two, else 0         */
+    int mode;         /* TermsMode                                          */
+};
+
 /* Per-scale statistic launch: all frames of a chunk, one CTA per strip. */
 struct StatsArgs {
     SrcDesc src;
     int w, h;          /* plane size at this scale                          */
     int nframes;
-    double nsq;
-    float gain_limit;
+    TermParams terms;
     float2 *rows;      /* row sums, (num, den)                              */
     int rows_stride;   /* float2 per frame in rows                          */
     int rows_base;     /* offset of this scale inside a frame's rows        */
@@ -66,6 +83,16 @@ struct FinalArgs {
 
 /* Taps of scale s for a kernelscale (host); FVIF_OK or FVIF_EINVAL. */
 int make_taps(float kernelscale, int s, Taps &out);
+
+/* Statistic constants for a noise variance (host).  mode is a TermsMode;
+ * outside [2^-60, 2^60] the pair evaluation is not used. */
+void make_term_params(double nsq, float gain_limit, int mode, TermParams &out);
+
+/* Per-pixel terms over arrays (diagnostics); fallbacks may be null. */
+cudaError_t launch_terms(const TermParams &tp, const float *mu1,
+                         const float *mu2, const float *xx, const float *yy,
+                         const float *xy, int n, float *num, float *den,
+                         unsigned long long *fallbacks, cudaStream_t st);
 
 cudaError_t launch_stats(const StatsArgs &a, const Taps &taps,
                          cudaStream_t st);

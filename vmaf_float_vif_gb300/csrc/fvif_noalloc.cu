@@ -122,6 +122,9 @@ extern "C" int fvif_score_noalloc(int w, int h, int bitdepth,
     float2 *rows = reinterpret_cast<float2 *>(scratch + rows_off);
     cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
 
+    TermParams terms;
+    make_term_params(sigma_nsq, 100.0f, kTermsPair, terms);
+
     SrcDesc s0;
     s0.kind = bitdepth == 8 ? SrcKind::U8 : SrcKind::U16;
     s0.scale = bitdepth == 8 ? 1.0f : 1.0f / (float)(1 << (bitdepth - 8));
@@ -169,8 +172,7 @@ extern "C" int fvif_score_noalloc(int w, int h, int bitdepth,
             a.w = ws[s];
             a.h = hs[s];
             a.nframes = 1;
-            a.nsq = sigma_nsq;
-            a.gain_limit = 100.0f;
+            a.terms = terms;
             a.rows = rows;
             a.rows_stride = rows_total;
             a.rows_base = rows_base[s];
