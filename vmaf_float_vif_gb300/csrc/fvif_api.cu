@@ -17,6 +17,7 @@ using namespace fvif;
 namespace {
 
 constexpr int kDefaultChunk = 16;
+constexpr int kLanes = 2; /* chunks alternate between two streams */
 
 thread_local int g_create_status = FVIF_OK;
 
@@ -41,8 +42,10 @@ int make_taps(float kernelscale, int s, Taps &out)
     const int r = (int)half;
     std::memset(&out, 0, sizeof out);
     out.n = 2 * r + 1;
+    out.one2 = make_float2(1.0f, 1.0f);
     if (r == 0) {
         out.t[0] = 1.0f;
+        out.t2[0] = make_float2(1.0f, 1.0f);
         return FVIF_OK;
     }
     const double sigma = ks * base / 5.0;
@@ -56,6 +59,8 @@ int make_taps(float kernelscale, int s, Taps &out)
     }
     for (int k = 0; k < out.n; ++k)
         out.t[k] = (float)(wk[k] / sum);
+    for (int k = 0; k < out.n; ++k)
+        out.t2[k] = make_float2(out.t[k], out.t[k]);
     return FVIF_OK;
 }
 
@@ -123,8 +128,16 @@ struct fvif_ctx {
     cudaStream_t stream = nullptr;
     int last_status = FVIF_OK;
 
-    float2 *pyr[kScales] = {};   /* scales 1..3, chunk frames each        */
-    float2 *rows = nullptr;      /* chunk frames x sum(h_s) (num, den)    */
+    /* Consecutive chunks alternate between two lanes, each with its own
+     * stream and buffers, so one chunk's small kernels overlap the next
+     * chunk's work.  Lanes fork from and join back into `stream`. */
+    struct Lane {
+        float2 *pyr[kScales] = {}; /* scales 1..3, chunk frames each      */
+        float2 *rows = nullptr;    /* chunk frames x sum(h_s) (num, den)  */
+        cudaStream_t stream = nullptr;
+        cudaEvent_t done = nullptr;
+    } lanes[kLanes];
+    cudaEvent_t fork = nullptr;
     int rows_stride = 0;
     int rows_base[kScales] = {};
     float2 *sums = nullptr;      /* chunk x 4 (diagnostics)               */
@@ -169,11 +182,19 @@ int cuda_status(cudaError_t e)
 
 void release(fvif_ctx *c)
 {
-    for (int s = 0; s < kScales; ++s)
-        if (c->pyr[s])
-            cudaFree(c->pyr[s]);
-    if (c->rows)
-        cudaFree(c->rows);
+    for (fvif_ctx::Lane &l : c->lanes) {
+        for (int s = 0; s < kScales; ++s)
+            if (l.pyr[s])
+                cudaFree(l.pyr[s]);
+        if (l.rows)
+            cudaFree(l.rows);
+        if (l.stream)
+            cudaStreamDestroy(l.stream);
+        if (l.done)
+            cudaEventDestroy(l.done);
+    }
+    if (c->fork)
+        cudaEventDestroy(c->fork);
     if (c->sums)
         cudaFree(c->sums);
     if (c->d_out)
@@ -196,7 +217,7 @@ void release(fvif_ctx *c)
 }
 
 /* Record the start event of one launch of kind k (profiling only). */
-cudaError_t prof_begin(fvif_ctx *c, int k)
+cudaError_t prof_begin(fvif_ctx *c, int k, cudaStream_t st)
 {
     c->launches[k] += 1;
     if (!c->profiling)
@@ -211,15 +232,15 @@ cudaError_t prof_begin(fvif_ctx *c, int k)
             v.push_back(ev);
         }
     }
-    return cudaEventRecord(v[c->prof_used[k]], c->stream);
+    return cudaEventRecord(v[c->prof_used[k]], st);
 }
 
-cudaError_t prof_end(fvif_ctx *c, int k)
+cudaError_t prof_end(fvif_ctx *c, int k, cudaStream_t st)
 {
     if (!c->profiling)
         return cudaSuccess;
-    cudaError_t e = cudaEventRecord(c->prof_events[k][c->prof_used[k] + 1],
-                                    c->stream);
+    cudaError_t e =
+        cudaEventRecord(c->prof_events[k][c->prof_used[k] + 1], st);
     c->prof_used[k] += 2;
     return e;
 }
@@ -236,11 +257,11 @@ SrcDesc scale0_src(const fvif_ctx *c, const void *ref, const void *dist)
     return d;
 }
 
-SrcDesc pyr_src(const fvif_ctx *c, int s)
+SrcDesc pyr_src(const fvif_ctx *c, const fvif_ctx::Lane &l, int s)
 {
     SrcDesc d;
     d.kind = SrcKind::F2;
-    d.x = c->pyr[s];
+    d.x = l.pyr[s];
     d.y = nullptr;
     d.scale = 1.0f;
     d.frame_elems = (size_t)c->ws[s] * c->hs[s];
@@ -249,47 +270,47 @@ SrcDesc pyr_src(const fvif_ctx *c, int s)
 
 /* One chunk (nf <= chunk frames) on the context stream: the pyramid, the
  * four statistic launches and the final reduction into out (device). */
-int run_chunk(fvif_ctx *c, const void *ref, const void *dist, int nf,
-              double *out, float2 *sums)
+int run_chunk(fvif_ctx *c, fvif_ctx::Lane &l, const void *ref,
+              const void *dist, int nf, double *out, float2 *sums)
 {
-    cudaStream_t st = c->stream;
+    cudaStream_t st = l.stream;
     const SrcDesc s0 = scale0_src(c, ref, dist);
     cudaError_t e = cudaSuccess;
 
     for (int s = 1; s < kScales && e == cudaSuccess; ++s) {
         DecArgs d;
-        d.src = (s == 1) ? s0 : pyr_src(c, s - 1);
+        d.src = (s == 1) ? s0 : pyr_src(c, l, s - 1);
         d.w = c->ws[s - 1];
         d.h = c->hs[s - 1];
         d.nframes = nf;
-        d.dst = c->pyr[s];
+        d.dst = l.pyr[s];
         d.dst_frame_elems = (size_t)c->ws[s] * c->hs[s];
-        e = prof_begin(c, FVIF_K_DECIMATE);
+        e = prof_begin(c, FVIF_K_DECIMATE, st);
         if (e == cudaSuccess)
             e = launch_decimate(d, c->taps[s], st);
         if (e == cudaSuccess)
-            e = prof_end(c, FVIF_K_DECIMATE);
+            e = prof_end(c, FVIF_K_DECIMATE, st);
     }
     for (int s = 0; s < kScales && e == cudaSuccess; ++s) {
         StatsArgs a;
-        a.src = (s == 0) ? s0 : pyr_src(c, s);
+        a.src = (s == 0) ? s0 : pyr_src(c, l, s);
         a.w = c->ws[s];
         a.h = c->hs[s];
         a.nframes = nf;
         a.terms = c->terms;
-        a.rows = c->rows;
+        a.rows = l.rows;
         a.rows_stride = c->rows_stride;
         a.rows_base = c->rows_base[s];
         const int kind = s == 0 ? FVIF_K_STATS0 : FVIF_K_STATS123;
-        e = prof_begin(c, kind);
+        e = prof_begin(c, kind, st);
         if (e == cudaSuccess)
             e = launch_stats(a, c->taps[s], st);
         if (e == cudaSuccess)
-            e = prof_end(c, kind);
+            e = prof_end(c, kind, st);
     }
     if (e == cudaSuccess) {
         FinalArgs f;
-        f.rows = c->rows;
+        f.rows = l.rows;
         f.rows_stride = c->rows_stride;
         for (int s = 0; s < kScales; ++s) {
             f.rows_base[s] = c->rows_base[s];
@@ -298,29 +319,51 @@ int run_chunk(fvif_ctx *c, const void *ref, const void *dist, int nf,
         f.nframes = nf;
         f.out = out;
         f.sums = sums;
-        e = prof_begin(c, FVIF_K_FINAL);
+        e = prof_begin(c, FVIF_K_FINAL, st);
         if (e == cudaSuccess)
             e = launch_final(f, st);
         if (e == cudaSuccess)
-            e = prof_end(c, FVIF_K_FINAL);
+            e = prof_end(c, FVIF_K_FINAL, st);
     }
     return cuda_status(e);
+}
+
+/* The lanes start after everything already queued on the context stream. */
+cudaError_t fork_lanes(fvif_ctx *c)
+{
+    cudaError_t e = cudaEventRecord(c->fork, c->stream);
+    for (int i = 0; i < kLanes && e == cudaSuccess; ++i)
+        e = cudaStreamWaitEvent(c->lanes[i].stream, c->fork, 0);
+    return e;
+}
+
+/* Work queued on the context stream afterwards waits for both lanes. */
+cudaError_t join_lanes(fvif_ctx *c)
+{
+    cudaError_t e = cudaSuccess;
+    for (int i = 0; i < kLanes && e == cudaSuccess; ++i) {
+        e = cudaEventRecord(c->lanes[i].done, c->lanes[i].stream);
+        if (e == cudaSuccess)
+            e = cudaStreamWaitEvent(c->stream, c->lanes[i].done, 0);
+    }
+    return e;
 }
 
 int enqueue_all(fvif_ctx *c, const void *ref, const void *dist, int n,
                 double *out)
 {
     const size_t fb = c->frame_bytes();
-    for (int f0 = 0; f0 < n; f0 += c->chunk) {
+    int st = cuda_status(fork_lanes(c));
+    int i = 0;
+    for (int f0 = 0; f0 < n && st == FVIF_OK; f0 += c->chunk, ++i) {
         const int nf = (n - f0 < c->chunk) ? n - f0 : c->chunk;
-        const int st =
-            run_chunk(c, static_cast<const unsigned char *>(ref) + fb * f0,
-                      static_cast<const unsigned char *>(dist) + fb * f0, nf,
-                      out + (size_t)kScales * f0, nullptr);
-        if (st != FVIF_OK)
-            return st;
+        st = run_chunk(c, c->lanes[i % kLanes],
+                       static_cast<const unsigned char *>(ref) + fb * f0,
+                       static_cast<const unsigned char *>(dist) + fb * f0, nf,
+                       out + (size_t)kScales * f0, nullptr);
     }
-    return FVIF_OK;
+    const int sj = cuda_status(join_lanes(c));
+    return st != FVIF_OK ? st : sj;
 }
 
 int ensure_out(fvif_ctx *c, int n)
@@ -433,12 +476,21 @@ fvif_ctx *fvif_create(int w, int h, int bitdepth, float kernelscale,
         rows_total += c->hs[s];
     }
     c->rows_stride = rows_total;
-    for (int s = 1; s < kScales && e == cudaSuccess; ++s)
-        e = cudaMalloc(&c->pyr[s], sizeof(float2) * (size_t)c->ws[s] *
-                                       c->hs[s] * c->chunk);
+    for (int i = 0; i < kLanes && e == cudaSuccess; ++i) {
+        fvif_ctx::Lane &l = c->lanes[i];
+        for (int s = 1; s < kScales && e == cudaSuccess; ++s)
+            e = cudaMalloc(&l.pyr[s], sizeof(float2) * (size_t)c->ws[s] *
+                                          c->hs[s] * c->chunk);
+        if (e == cudaSuccess)
+            e = cudaMalloc(&l.rows,
+                           sizeof(float2) * (size_t)rows_total * c->chunk);
+        if (e == cudaSuccess)
+            e = cudaStreamCreateWithFlags(&l.stream, cudaStreamNonBlocking);
+        if (e == cudaSuccess)
+            e = cudaEventCreateWithFlags(&l.done, cudaEventDisableTiming);
+    }
     if (e == cudaSuccess)
-        e = cudaMalloc(&c->rows,
-                       sizeof(float2) * (size_t)rows_total * c->chunk);
+        e = cudaEventCreateWithFlags(&c->fork, cudaEventDisableTiming);
     if (e == cudaSuccess)
         e = cudaMalloc(&c->sums, sizeof(float2) * kScales * (size_t)c->chunk);
     int st = cuda_status(e);
@@ -460,6 +512,9 @@ void fvif_destroy(fvif_ctx *ctx)
         return;
     DeviceGuard g(ctx->device);
     cudaStreamSynchronize(ctx->stream);
+    for (fvif_ctx::Lane &l : ctx->lanes)
+        if (l.stream)
+            cudaStreamSynchronize(l.stream);
     release(ctx);
     delete ctx;
 }
@@ -497,6 +552,9 @@ int fvif_profile_enable(fvif_ctx *ctx, int enable)
     DeviceGuard g(ctx->device);
     if (cudaStreamSynchronize(ctx->stream) != cudaSuccess)
         return set_status(ctx, FVIF_ECUDA);
+    for (fvif_ctx::Lane &l : ctx->lanes)
+        if (cudaStreamSynchronize(l.stream) != cudaSuccess)
+            return set_status(ctx, FVIF_ECUDA);
     ctx->profiling = enable != 0;
     for (int k = 0; k < FVIF_K_COUNT; ++k) {
         ctx->prof_used[k] = 0;
@@ -597,12 +655,14 @@ int fvif_score_host(fvif_ctx *ctx, const void *ref, const void *dist,
 
     const size_t fb = ctx->frame_bytes();
     const size_t half = fb * (size_t)ctx->chunk;
-    cudaError_t e = cudaSuccess;
+    cudaError_t e = fork_lanes(ctx);
     int i = 0;
     for (int f0 = 0; f0 < n_frames && e == cudaSuccess; f0 += ctx->chunk, ++i) {
         const int nf = (n_frames - f0 < ctx->chunk) ? n_frames - f0
                                                     : ctx->chunk;
-        const int slot = i & 1;
+        /* staging slot i % 2 is scored on lane i % 2 */
+        const int slot = i % kLanes;
+        fvif_ctx::Lane &lane = ctx->lanes[slot];
         unsigned char *dref = ctx->stage[slot];
         unsigned char *ddist = ctx->stage[slot] + half;
         /* the slot is free once the chunk that used it two steps ago ran */
@@ -622,18 +682,21 @@ int fvif_score_host(fvif_ctx *ctx, const void *ref, const void *dist,
         if (e == cudaSuccess)
             e = cudaEventRecord(ctx->copied[slot], ctx->copy_stream);
         if (e == cudaSuccess)
-            e = cudaStreamWaitEvent(ctx->stream, ctx->copied[slot], 0);
+            e = cudaStreamWaitEvent(lane.stream, ctx->copied[slot], 0);
         if (e != cudaSuccess)
             break;
-        st = run_chunk(ctx, dref, ddist, nf,
+        st = run_chunk(ctx, lane, dref, ddist, nf,
                        ctx->d_out + (size_t)kScales * f0, nullptr);
         if (st != FVIF_OK)
-            return set_status(ctx, st);
-        e = cudaEventRecord(ctx->consumed[slot], ctx->stream);
+            break;
+        e = cudaEventRecord(ctx->consumed[slot], lane.stream);
     }
-    if (e != cudaSuccess) {
+    const cudaError_t ej = join_lanes(ctx);
+    if (e != cudaSuccess || st != FVIF_OK || ej != cudaSuccess) {
         cudaStreamSynchronize(ctx->copy_stream);
-        return set_status(ctx, cuda_status(e));
+        cudaStreamSynchronize(ctx->stream);
+        return set_status(ctx, st != FVIF_OK ? st
+                               : cuda_status(e != cudaSuccess ? e : ej));
     }
     return set_status(ctx, finish_to_host(ctx, n_frames, out));
 }
@@ -668,7 +731,13 @@ int fvif_debug_frame(fvif_ctx *ctx, const void *ref, const void *dist,
     DeviceGuard g(ctx->device);
     if (!g.ok)
         return set_status(ctx, FVIF_ECUDA);
-    const int st = run_chunk(ctx, ref, dist, 1, ctx->d_out, ctx->sums);
+    fvif_ctx::Lane &lane = ctx->lanes[0];
+    int st = cuda_status(fork_lanes(ctx));
+    if (st == FVIF_OK)
+        st = run_chunk(ctx, lane, ref, dist, 1, ctx->d_out, ctx->sums);
+    const int sj = cuda_status(join_lanes(ctx));
+    if (st == FVIF_OK)
+        st = sj;
     if (st != FVIF_OK)
         return set_status(ctx, st);
     cudaError_t e = cudaSuccess;
@@ -682,7 +751,7 @@ int fvif_debug_frame(fvif_ctx *ctx, const void *ref, const void *dist,
         for (int s = 0; s < kScales && e == cudaSuccess; ++s) {
             const size_t np = (size_t)ctx->ws[s] * ctx->hs[s];
             const SrcDesc d = s == 0 ? scale0_src(ctx, ref, dist)
-                                     : pyr_src(ctx, s);
+                                     : pyr_src(ctx, lane, s);
             e = launch_unpack_planes(d, ctx->ws[s], ctx->hs[s], tmp + off,
                                      tmp + off + np, ctx->stream);
             off += 2 * np;
@@ -700,7 +769,7 @@ int fvif_debug_frame(fvif_ctx *ctx, const void *ref, const void *dist,
     if (rows) {
         size_t off = 0;
         for (int s = 0; s < kScales && e == cudaSuccess; ++s) {
-            e = cudaMemcpyAsync(rows + off, ctx->rows + ctx->rows_base[s],
+            e = cudaMemcpyAsync(rows + off, lane.rows + ctx->rows_base[s],
                                 sizeof(float2) * ctx->hs[s],
                                 cudaMemcpyDeviceToHost, ctx->stream);
             off += 2 * (size_t)ctx->hs[s];

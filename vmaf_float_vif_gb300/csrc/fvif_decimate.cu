@@ -72,10 +72,18 @@ cudaError_t launch_decimate(const DecArgs &a, const Taps &tp, cudaStream_t st)
 /* One warp per (frame, scale): the row sums added top to bottom into one
  * fp32 accumulator per output, then vif_scale = num / den in fp64
  * ("ADR-1422 ...", Decision: the rows' sums are added top to bottom in
- * fp32).  Every lane carries the same running sums; lane 0 writes. */
-__global__ void final_kernel(const FinalArgs a)
+ * fp32).  The warp stages 256 rows at a time in shared memory; lane 0 adds
+ * them in order (the loads are independent of the sum chain, so they
+ * pipeline). */
+constexpr int kFinalWarps = 4;
+constexpr int kFinalBatch = 256;
+
+__global__ void __launch_bounds__(32 * kFinalWarps)
+    final_kernel(const FinalArgs a)
 {
-    const int warp = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+    __shared__ float2 buf[kFinalWarps][kFinalBatch];
+    const int wib = threadIdx.x >> 5;
+    const int warp = blockIdx.x * kFinalWarps + wib;
     const int lane = threadIdx.x & 31;
     if (warp >= a.nframes * kScales)
         return;
@@ -83,13 +91,20 @@ __global__ void final_kernel(const FinalArgs a)
     const int h = a.h[s];
     const float2 *r = a.rows + (size_t)f * a.rows_stride + a.rows_base[s];
     float num = 0.0f, den = 0.0f;
-    for (int b = 0; b < h; b += 32) {
-        const float2 v = (b + lane < h) ? r[b + lane] : make_float2(0.f, 0.f);
-        const int cnt = min(32, h - b);
-        for (int j = 0; j < cnt; ++j) {
-            num = __fadd_rn(num, __shfl_sync(0xffffffffu, v.x, j));
-            den = __fadd_rn(den, __shfl_sync(0xffffffffu, v.y, j));
+    for (int b = 0; b < h; b += kFinalBatch) {
+        const int cnt = min(kFinalBatch, h - b);
+        for (int j = lane; j < cnt; j += 32)
+            buf[wib][j] = r[b + j];
+        __syncwarp();
+        if (lane == 0) {
+#pragma unroll 8
+            for (int j = 0; j < cnt; ++j) {
+                const float2 v = buf[wib][j];
+                num = __fadd_rn(num, v.x);
+                den = __fadd_rn(den, v.y);
+            }
         }
+        __syncwarp();
     }
     if (lane == 0) {
         a.out[(size_t)f * kScales + s] = __ddiv_rn((double)num, (double)den);
@@ -101,8 +116,8 @@ __global__ void final_kernel(const FinalArgs a)
 cudaError_t launch_final(const FinalArgs &a, cudaStream_t st)
 {
     const int warps = a.nframes * kScales;
-    const int threads = 128;
-    const int blocks = (warps * 32 + threads - 1) / threads;
+    const int threads = 32 * kFinalWarps;
+    const int blocks = (warps + kFinalWarps - 1) / kFinalWarps;
     final_kernel<<<blocks, threads, 0, st>>>(a);
     return cudaGetLastError();
 }

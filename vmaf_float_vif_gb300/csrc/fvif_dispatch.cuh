@@ -51,7 +51,8 @@ cudaError_t run_decimate(const DecArgs &a, const Taps &tp, cudaStream_t st)
     cudaError_t e = ensure_smem(decimate_kernel<N, K>, max_bytes, done);
     if (e != cudaSuccess)
         return e;
-    const dim3 grid((unsigned)((a.w / 2 + kDX - 1) / kDX),
+    const int dx = dec_cols(r);
+    const dim3 grid((unsigned)((a.w / 2 + dx - 1) / dx),
                     (unsigned)((a.h / 2 + kDY - 1) / kDY), (unsigned)a.nframes);
     decimate_kernel<N, K><<<grid, kDecThreads, dec_smem_bytes(r), st>>>(a, tp);
     return cudaGetLastError();

@@ -18,6 +18,8 @@ constexpr int kMaxTaps = 2 * kMaxRadius + 1; /* 129                          */
  * so compile-time-indexed reads become constant-bank operands.            */
 struct Taps {
     float t[kMaxTaps];
+    float2 t2[kMaxTaps]; /* (t[k], t[k]) for the packed two-lane operations */
+    float2 one2;         /* (1, 1), read at run time (see acc2_rn)          */
     int n;
 };
 
