@@ -202,6 +202,22 @@ def stats_ops_per_pixel(ntaps: int) -> int:
     return 10 * (2 * ntaps - 1) + 3
 
 
+def frame_ops(w: int, h: int, taps) -> int:
+    """Algorithmic fp32 filter operations of one frame pair over the four
+    scales: the statistic filters, and each decimation's vertical pass at
+    the kept rows and horizontal pass at the kept samples (two planes)."""
+    ops = 0
+    ws, hs = w, h
+    for s in range(4):
+        if s > 0:
+            n = taps[s]
+            w2, h2 = ws // 2, hs // 2
+            ops += 2 * (2 * n - 1) * (h2 * ws + h2 * w2)
+            ws, hs = w2, h2
+        ops += ws * hs * stats_ops_per_pixel(taps[s])
+    return ops
+
+
 def run_ours(args):
     import torch
     import vmaf_float_vif_gb300 as fv
@@ -326,6 +342,8 @@ def run_ours(args):
     clk = clocks.summary()
     sm_max = clk.get("sm_max_mhz") or peaks.get("sm_max_mhz") or 2070.0
 
+    taps = [len(ctx.taps(s)) for s in range(4)]
+    step_ops = frames * frame_ops(case.w, case.h, taps)
     st0_ms, st0_n = prof["stats_scale0"]
     launches_total = sum(n for _, n in prof.values())
     px0 = case.w * case.h
@@ -357,7 +375,7 @@ def run_ours(args):
             "workload": describe(args.workload, args.frames),
             "frames_per_step": frames,
             "chunk_frames": chunk,
-            "taps": [len(ctx.taps(s)) for s in range(4)],
+            "taps": taps,
             "l2": "no flush: inputs %.2f GB per step exceed the 129 MB L2" %
                   (frames * bpp / 1e9),
             "hbm_fraction_algorithmic": value / world * bpp / 1e9 / hbm_peak,
@@ -379,11 +397,20 @@ def run_ours(args):
             "peak_note": "%d SMs x %d fp32 lanes x %.0f MHz, one non-fused op "
                          "per lane per clock" % (SMS, FP32_LANES_PER_SM,
                                                  sm_max),
+            "launch_note": "events on the launching stream; consecutive chunks "
+                           "run on two streams, so a launch shares the GPU "
+                           "with the other chunk's smaller kernels",
+            "step_achieved": step_ops / (ms_step / 1e3) / 1e12,
+            "step_frac": step_ops / (ms_step / 1e3) / 1e12 / alu_peak,
+            "step_note": "all algorithmic filter operations of a step (%.3g "
+                         "per frame pair) / step time" % (step_ops / frames),
         },
         "gpu_launches": int(launches_total),
         "clocks": clk,
     }
     ctx.close()
+    if args.also and args.also != args.workload:
+        line["also"] = secondary(args.also, args)
     if e2e:
         line["e2e"] = e2e
     if not args.no_cpu_baseline:
@@ -398,6 +425,36 @@ def run_ours(args):
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def secondary(name, args):
+    """Device-resident throughput of a second workload (same timing)."""
+    import torch
+    import vmaf_float_vif_gb300 as fv
+    case, (ref, dist_np) = make_inputs(name)
+    _, frames, ks = WORKLOADS[name]
+
+    def as_dev(a):
+        return torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16
+                                else a).to("cuda")
+    r, d = as_dev(ref), as_dev(dist_np)
+    out = torch.empty(4 * frames, dtype=torch.float64, device="cuda")
+    stream = torch.cuda.Stream()
+    with fv.Context(case.w, case.h, case.bitdepth, ks, case.nsq) as ctx:
+        ctx.set_stream(stream)
+        for _ in range(args.warmup):
+            ctx.score_async(r, d, out)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            ctx.score_async(r, d, out)
+        e1.record(stream)
+        torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    return {"workload": describe(name), "value": frames / (ms / 1e3),
+            "unit": "frame-pairs/s", "ms_per_step": ms}
 
 
 def run_reference(args):
@@ -464,6 +521,9 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--also", choices=sorted(WORKLOADS) + [""],
+                    default="c2_1080p_10b",
+                    help="second workload timed device-resident (\"\" = none)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("note: fewer than 3 warm-up steps", file=sys.stderr)
