@@ -81,6 +81,27 @@ def dist_env():
             int(os.environ.get("WORLD_SIZE", "1")))
 
 
+def max_over_ranks(x: float, world: int) -> float:
+    """The largest value of x over all ranks (the job's step time is its
+    slowest rank's).  The only collective of a multi-GPU run besides the
+    barriers; frame pairs never leave their GPU."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(frames_per_rank: int, steps: int, world: int,
+                   seconds: float) -> float:
+    """Whole-job frame pairs per second: every rank scores its own
+    frames_per_rank each step (weak scaling)."""
+    return frames_per_rank * steps * world / seconds
+
+
 # ---------------------------------------------------------------------------
 # clocks during the timed region
 
@@ -272,17 +293,23 @@ def run_ours(args):
     ms_total = start.elapsed_time(stop)
     prof = ctx.profile_read()
     ctx.profile(False)
+    # one chunk alone (after the timed region): its launches share the GPU
+    # with nothing, which gives the dominant kernel's standalone duration
+    n_solo = min(ctx.chunk_frames, frames)
+    out_solo = torch.empty(4 * n_solo, dtype=torch.float64, device="cuda")
+    ctx.profile(True)
+    for _ in range(3):
+        ctx.score_async(r_dev[:n_solo], d_dev[:n_solo], out_solo)
+    solo = ctx.profile_read()
+    ctx.profile(False)
+    solo_ms = solo["stats_scale0"][0] / max(1, solo["stats_scale0"][1])
     scores = out.cpu().numpy().reshape(-1, 4)
     if not np.all(np.isfinite(scores)):
         raise RuntimeError("non-finite scores")
 
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms_total], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(ms_total, world)
     ms_step = ms_total / args.steps
-    value = frames * args.steps * world / (ms_total / 1e3)
+    value = job_throughput(frames, args.steps, world, ms_total / 1e3)
 
     # e2e: host buffers, copies inside the timed region
     e2e = None
@@ -309,14 +336,10 @@ def run_ours(args):
         torch.cuda.synchronize()
         wall = time.perf_counter() - t0
         barrier()
-        if world > 1:
-            import torch.distributed as dist
-            t = torch.tensor([wall], dtype=torch.float64, device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            wall = float(t.item())
+        wall = max_over_ranks(wall, world)
         if not np.array_equal(host_scores, scores):
             raise RuntimeError("fvif_score_host and fvif_score_async differ")
-        e2e = {"value": frames * args.e2e_steps * world / wall,
+        e2e = {"value": job_throughput(frames, args.e2e_steps, world, wall),
                "unit": "frame-pairs/s",
                "h2d_bytes_per_step": int(ref.nbytes + dist_np.nbytes),
                "d2h_bytes_per_step": int(scores.nbytes),
@@ -400,6 +423,12 @@ def run_ours(args):
             "launch_note": "events on the launching stream; consecutive chunks "
                            "run on two streams, so a launch shares the GPU "
                            "with the other chunk's smaller kernels",
+            "solo_launch_ms": solo_ms,
+            "solo_achieved": ops_launch / (solo_ms / 1e3) / 1e12,
+            "solo_frac": ops_launch / (solo_ms / 1e3) / 1e12 / alu_peak,
+            "solo_note": "the same launch with no other chunk in flight "
+                         "(one 16-frame chunk scored alone after the timed "
+                         "region, events on its stream)",
             "step_achieved": step_ops / (ms_step / 1e3) / 1e12,
             "step_frac": step_ops / (ms_step / 1e3) / 1e12 / alu_peak,
             "step_note": "all algorithmic filter operations of a step (%.3g "
