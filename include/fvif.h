@@ -66,6 +66,28 @@ enum fvif_status {
 fvif_ctx *fvif_create(int w, int h, int bitdepth, float kernelscale,
                       double sigma_nsq);
 
+/* The extractor's options ("ADR-1422 ...", Decision and Consequences; "ADR-1444
+ * ...", Consequences name vif_enhn_gain_limit, vif_skip_scale0 and
+ * vif_scale1/2/3_min_val; their semantics here are this library's readings):
+ *  enhn_gain_limit : cap on the gain g (default 100).
+ *  skip_scale0     : nonzero -> scale 0 contributes nothing: its sums and
+ *                    vif_scale0 are 0 (default 0).
+ *  min_val[s]      : for s = 1..3, vif_scale_s = max(vif_scale_s, min_val[s])
+ *                    (defaults 0; min_val[0] is ignored). */
+typedef struct fvif_options {
+    float enhn_gain_limit;
+    int skip_scale0;
+    double min_val[4];
+} fvif_options;
+
+/* Fill *opt with the defaults above. */
+void fvif_default_options(fvif_options *opt);
+
+/* fvif_create with options (opt == NULL: defaults).  enhn_gain_limit must
+ * be > 0 and finite, each min_val finite. */
+fvif_ctx *fvif_create_ex(int w, int h, int bitdepth, float kernelscale,
+                         double sigma_nsq, const fvif_options *opt);
+
 /* Score n_frames frame pairs whose samples are in DEVICE memory (caller
  * owned, readable for the whole call).  out: HOST memory of 4*n_frames
  * doubles.  Synchronous: returns after out is written.  n_frames == 0 is a
@@ -87,6 +109,16 @@ int fvif_score_async(fvif_ctx *ctx, const void *ref, const void *dist,
  * work, slower).  out: HOST memory of 4*n_frames doubles.  Synchronous. */
 int fvif_score_host(fvif_ctx *ctx, const void *ref, const void *dist,
                     int n_frames, double *out);
+
+/* As fvif_score, with the fifteen debug outputs per frame in HOST memory
+ * (out: 15*n_frames doubles, frame-major): vif_scale0..3, the frame ratio
+ * vif = vif_num / vif_den, vif_num and vif_den (sums over the scales of the
+ * per-scale sums, in fp64, scale 0 first), then num_scale0..3 and
+ * den_scale0..3 (the per-scale fp32 sums).  "ADR-1444 ...", Consequences:
+ * the debug mode emits fifteen outputs, the frame ratio and every per-scale
+ * sum; the order and the fp64 totals are this library's reading. */
+int fvif_score_debug(fvif_ctx *ctx, const void *ref, const void *dist,
+                     int n_frames, double *out);
 
 /* Free the context and everything it allocated.  NULL is a no-op. */
 void fvif_destroy(fvif_ctx *ctx);

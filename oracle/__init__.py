@@ -98,6 +98,11 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
         ctypes.c_int, ctypes.c_float, ctypes.c_double, ctypes.c_float,
         _f64p, _f32p, _f32p, _f32p]
     lib.fvo_frame_ex.restype = ctypes.c_int
+    lib.fvo_frame_opts.argtypes = [
+        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
+        ctypes.c_int, ctypes.c_float, ctypes.c_double, ctypes.c_float,
+        ctypes.c_int, _f64p, _f64p, _f64p]
+    lib.fvo_frame_opts.restype = ctypes.c_int
     lib.fvo_score.argtypes = [
         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
         ctypes.c_int, ctypes.c_float, ctypes.c_double, ctypes.c_int, _f64p]
@@ -226,6 +231,28 @@ def frame(ref: np.ndarray, dist: np.ndarray, bitdepth: int,
                               planes[po + n:po + 2 * n].reshape(hs, ws)))
         po += 2 * n
     return out
+
+
+def frame_opts(ref: np.ndarray, dist: np.ndarray, bitdepth: int,
+               kernelscale: float, nsq: float,
+               gain_limit: float = DEFAULT_GAIN_LIMIT, skip_scale0=False,
+               min_val=(0.0, 0.0, 0.0, 0.0), L=None):
+    """One frame pair with the extractor's options: (scores[4], debug[15])."""
+    L = L or lib()
+    dt = np.uint8 if bitdepth == 8 else np.uint16
+    ref = np.ascontiguousarray(ref, dt)
+    dist = np.ascontiguousarray(dist, dt)
+    h, w = ref.shape
+    mv = np.ascontiguousarray(min_val, np.float64)
+    scores = np.zeros(4, np.float64)
+    dbg = np.zeros(15, np.float64)
+    rc = L.fvo_frame_opts(ref.ctypes.data, dist.ctypes.data, w, h, bitdepth,
+                          float(kernelscale), float(nsq), float(gain_limit),
+                          1 if skip_scale0 else 0, _dptr(mv), _dptr(scores),
+                          _dptr(dbg))
+    if rc:
+        raise ValueError("oracle rejected the frame (rc=%d)" % rc)
+    return scores, dbg
 
 
 def score(ref: np.ndarray, dist: np.ndarray, bitdepth: int,

@@ -384,6 +384,58 @@ int fvo_frame_ex(const void *ref, const void *dist, int w, int h, int bd,
     return 0;
 }
 
+/* The extractor's options and debug outputs.  "ADR-1422 ...", Decision and
+ * Consequences, and "ADR-1444 ...", Consequences, name the option table
+ * (vif_enhn_gain_limit, vif_skip_scale0, vif_scale1/2/3_min_val) and a
+ * debug mode with fifteen outputs, the frame ratio and every per-scale sum;
+ * their semantics are readings:
+ *  - skip_scale0: scale 0 contributes nothing: num_0 = den_0 = 0 and
+ *    vif_scale0 = 0 (scale 1 is still decimated from the scale-0 plane);
+ *  - min_val[s] (s = 1..3): vif_scale_s = max(vif_scale_s, min_val[s]);
+ *  - debug (15 doubles): vif_scale0..3 (floored), vif = vif_num / vif_den,
+ *    vif_num = sum over s of num_s, vif_den likewise (fp64, s ascending),
+ *    then num_0..3 and den_0..3 (the per-scale fp32 sums). */
+int fvo_frame_opts(const void *ref, const void *dist, int w, int h, int bd,
+                   float kernelscale, double nsq, float gain_limit,
+                   int skip_scale0, const double *min_val, double *scores,
+                   double *debug15)
+{
+    float sums[8];
+    double raw[4];
+    int rc = fvo_frame_ex(ref, dist, w, h, bd, kernelscale, nsq, gain_limit,
+                          raw, NULL, sums, NULL);
+    if (rc)
+        return rc;
+    if (skip_scale0) {
+        sums[0] = 0.0f;
+        sums[1] = 0.0f;
+        raw[0] = 0.0;
+    }
+    for (int s = 0; s < NSCALES; ++s) {
+        double v = raw[s];
+        if (s > 0 && min_val && v < min_val[s])
+            v = min_val[s];
+        scores[s] = v;
+    }
+    if (debug15) {
+        double num = 0.0, den = 0.0;
+        for (int s = 0; s < NSCALES; ++s) {
+            num = num + (double)sums[2 * s];
+            den = den + (double)sums[2 * s + 1];
+        }
+        for (int s = 0; s < NSCALES; ++s)
+            debug15[s] = scores[s];
+        debug15[4] = num / den;
+        debug15[5] = num;
+        debug15[6] = den;
+        for (int s = 0; s < NSCALES; ++s) {
+            debug15[7 + s] = (double)sums[2 * s];
+            debug15[11 + s] = (double)sums[2 * s + 1];
+        }
+    }
+    return 0;
+}
+
 int fvo_frame(const void *ref, const void *dist, int w, int h, int bd,
               float kernelscale, double nsq, double *scores)
 {

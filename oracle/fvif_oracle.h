@@ -34,6 +34,10 @@ int fvo_plane_size(int w, int h, int scale, int *ws, int *hs);
 int fvo_frame_ex(const void *ref, const void *dist, int w, int h, int bd,
                  float kernelscale, double nsq, float gain_limit,
                  double *scores, float *rowsums, float *sums, float *planes);
+int fvo_frame_opts(const void *ref, const void *dist, int w, int h, int bd,
+                   float kernelscale, double nsq, float gain_limit,
+                   int skip_scale0, const double *min_val, double *scores,
+                   double *debug15);
 int fvo_frame(const void *ref, const void *dist, int w, int h, int bd,
               float kernelscale, double nsq, double *scores);
 int fvo_score(const void *ref, const void *dist, int w, int h, int bd,

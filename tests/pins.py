@@ -534,6 +534,46 @@ def pin_sum_order(L):
         assert det["scores"][s] == float(tn) / float(td), s
 
 
+def pin_gain_limit_option(L):
+    """A gain limit of 1 caps g = 2 (dist = 2 ref) before the term and after
+    sv: sv = 4 s1 - 2 (2 s1) -> eps, num = log2(1 + s1 / (eps + nsq))."""
+    for nsq in (2.0, 1.5):
+        s1 = 37.0
+        num, den = oracle.pixel_terms([0.0], [0.0], [s1], [4 * s1], [2 * s1],
+                                      nsq, 1.0, L=L)
+        want = math.log2(1.0 + s1 / (1e-10 + nsq))
+        assert _close(float(num[0]), want), (nsq, num, want)
+        num100, _ = oracle.pixel_terms([0.0], [0.0], [s1], [4 * s1],
+                                       [2 * s1], nsq, 100.0, L=L)
+        assert _close(float(num100[0]),
+                      math.log2(1.0 + 4 * s1 / (1e-10 + nsq)))
+
+
+def pin_options_and_debug(L):
+    """skip_scale0 zeroes scale 0 only; the floors clamp scales 1..3 from
+    below; the fifteen debug values satisfy their defining identities."""
+    from vmaf_float_vif_gb300 import synthetic as S
+    case = S.custom_noise_case(96, 80, 8)
+    r, d = case.pair(0)
+    base, dbg = oracle.frame_opts(r, d, 8, 1.0, 2.0, L=L)
+    plain = oracle.frame(r, d, 8, 1.0, 2.0, L=L)
+    assert np.array_equal(base, plain)
+    assert np.array_equal(dbg[:4], base)
+    nums, dens = dbg[7:11], dbg[11:15]
+    assert np.array_equal(base, nums / dens)
+    assert dbg[5] == ((nums[0] + nums[1]) + nums[2]) + nums[3]
+    assert dbg[6] == ((dens[0] + dens[1]) + dens[2]) + dens[3]
+    assert dbg[4] == dbg[5] / dbg[6]
+    sk, dsk = oracle.frame_opts(r, d, 8, 1.0, 2.0, skip_scale0=True, L=L)
+    assert sk[0] == 0.0 and np.array_equal(sk[1:], base[1:])
+    assert dsk[7] == 0.0 and dsk[11] == 0.0
+    assert dsk[4] == (dsk[5] / dsk[6]) and dsk[5] == (nums[1] + nums[2]) + nums[3]
+    floors = (0.0, 0.99, 0.0, 2.0)
+    fl, _ = oracle.frame_opts(r, d, 8, 1.0, 2.0, min_val=floors, L=L)
+    assert fl[0] == base[0] and fl[2] == base[2]
+    assert fl[1] == max(base[1], 0.99) and fl[3] == 2.0
+
+
 ALL_PINS = [
     pin_tap_widths, pin_taps_symmetric_normalised, pin_taps_gaussian,
     pin_mirror_table, pin_mirror_exhaustive, pin_filter_brute,
@@ -544,4 +584,5 @@ ALL_PINS = [
     pin_log2_exact_powers, pin_log2_error_bound, pin_log2_monotone,
     pin_identical_frames, pin_black_frames_exactly_one,
     pin_flat_ref_closed_form, pin_textbook_vif, pin_sum_order,
+    pin_gain_limit_option, pin_options_and_debug,
 ]

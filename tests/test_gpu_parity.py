@@ -231,3 +231,42 @@ def test_chunk_size_override(fv, monkeypatch):
         assert ctx.chunk_frames == 3
         got = ctx.score(to_device(ref), to_device(dist))
     assert_bitwise(got, oracle_scores(ref, dist, 8, 1.0, 2.0), "chunk 3")
+
+
+OPTION_SETS = [
+    dict(gain_limit=1.0),
+    dict(skip_scale0=True),
+    dict(min_val=(0.0, 0.99, 0.5, 2.0)),
+    dict(gain_limit=1.0, skip_scale0=True, min_val=(0.0, 0.3, 0.3, 0.3)),
+]
+
+
+@pytest.mark.parametrize("opts", OPTION_SETS,
+                         ids=["gain1", "skip0", "floors", "all"])
+@pytest.mark.parametrize("nsq", [2.0, 1.5, 4.7])
+def test_options_and_debug_outputs(fv, opts, nsq):
+    """The option table and the fifteen debug outputs, bit for bit."""
+    case = S.custom_noise_case(300, 170, 10, frames=3)
+    ref, dist = case.batch(range(3))
+    r, d = to_device(ref), to_device(dist)
+    with fv.Context(case.w, case.h, 10, 1.0, nsq, **opts) as ctx:
+        dbg = ctx.score_debug(r, d)
+        sc = ctx.score(r, d)
+    for f in range(3):
+        want_sc, want_dbg = oracle.frame_opts(
+            ref[f], dist[f], 10, 1.0, nsq,
+            gain_limit=opts.get("gain_limit", 100.0),
+            skip_scale0=opts.get("skip_scale0", False),
+            min_val=opts.get("min_val", (0.0, 0.0, 0.0, 0.0)))
+        assert_bitwise(sc[f], want_sc, "scores %s f%d" % (opts, f))
+        assert_bitwise(dbg[f], want_dbg, "debug %s f%d" % (opts, f))
+
+
+def test_debug_outputs_default_options(fv):
+    case = S.CASES["c1_576x324_8b"]
+    ref, dist = case.batch(range(case.frames))
+    with fv.Context(case.w, case.h, 8, 1.0, 2.0) as ctx:
+        dbg = ctx.score_debug(to_device(ref), to_device(dist))
+    for f in range(case.frames):
+        _, want = oracle.frame_opts(ref[f], dist[f], 8, 1.0, 2.0)
+        assert_bitwise(dbg[f], want, "debug c1 f%d" % f)

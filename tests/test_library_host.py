@@ -82,3 +82,23 @@ def test_missing_library_raises(monkeypatch, tmp_path):
     monkeypatch.setattr(_lib, "_lib", None)
     with pytest.raises(RuntimeError, match="not built"):
         _lib.lib(str(tmp_path / "nope.so"))
+
+
+def test_default_options(L):
+    o = _lib.fvif_default_options()
+    assert o.enhn_gain_limit == 100.0 and o.skip_scale0 == 0
+    assert list(o.min_val) == [0.0, 0.0, 0.0, 0.0]
+
+
+@pytest.mark.parametrize("field,value", [
+    ("enhn_gain_limit", 0.0), ("enhn_gain_limit", -1.0),
+    ("enhn_gain_limit", float("inf")), ("enhn_gain_limit", float("nan")),
+    ("min_val", float("nan")), ("min_val", float("inf"))])
+def test_create_ex_rejects_invalid_options(L, field, value):
+    o = _lib.fvif_default_options()
+    if field == "min_val":
+        o.min_val[2] = value
+    else:
+        setattr(o, field, value)
+    assert not L.fvif_create_ex(64, 64, 8, 1.0, 2.0, ctypes.byref(o))
+    assert L.fvif_last_error(None) == fv.FVIF_EINVAL

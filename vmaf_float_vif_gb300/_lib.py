@@ -28,8 +28,16 @@ EXPORTS = (
     "fvif_destroy", "fvif_set_stream", "fvif_last_error", "fvif_strerror",
     "fvif_chunk_frames", "fvif_get_taps", "fvif_debug_frame",
     "fvif_profile_enable", "fvif_profile_read", "fvif_score_noalloc",
-    "fvif_debug_terms",
+    "fvif_debug_terms", "fvif_default_options", "fvif_create_ex",
+    "fvif_score_debug",
 )
+
+
+class FvifOptions(ctypes.Structure):
+    """Mirror of struct fvif_options."""
+    _fields_ = [("enhn_gain_limit", ctypes.c_float),
+                ("skip_scale0", ctypes.c_int),
+                ("min_val", ctypes.c_double * 4)]
 
 FVIF_K_DECIMATE, FVIF_K_STATS0, FVIF_K_STATS123, FVIF_K_FINAL = range(4)
 KERNEL_KINDS = {"decimate": 0, "stats_scale0": 1, "stats_scale123": 2,
@@ -87,6 +95,12 @@ def _declare(L: ctypes.CDLL) -> ctypes.CDLL:
     L.fvif_profile_enable.restype = i
     L.fvif_profile_read.argtypes = [vp, i, dp, ctypes.POINTER(ctypes.c_longlong)]
     L.fvif_profile_read.restype = i
+    L.fvif_default_options.argtypes = [ctypes.POINTER(FvifOptions)]
+    L.fvif_default_options.restype = None
+    L.fvif_create_ex.argtypes = [i, i, i, f, d, ctypes.POINTER(FvifOptions)]
+    L.fvif_create_ex.restype = vp
+    L.fvif_score_debug.argtypes = [vp, vp, vp, i, vp]
+    L.fvif_score_debug.restype = i
     L.fvif_debug_terms.argtypes = [vp] + [vp] * 5 + [i, vp, vp, vp]
     L.fvif_debug_terms.restype = i
     L.fvif_score_noalloc.argtypes = [i, i, i, f, d, vp, vp, i, vp, vp]
@@ -161,6 +175,44 @@ def fvif_create(w: int, h: int, bitdepth: int, kernelscale: float,
     if not ctx:
         raise FvifError(L.fvif_last_error(None), "fvif_create")
     return ctx
+
+
+def fvif_default_options() -> FvifOptions:
+    o = FvifOptions()
+    lib().fvif_default_options(ctypes.byref(o))
+    return o
+
+
+def fvif_create_ex(w: int, h: int, bitdepth: int, kernelscale: float,
+                   sigma_nsq: float, gain_limit: float = 100.0,
+                   skip_scale0: bool = False,
+                   min_val=(0.0, 0.0, 0.0, 0.0)) -> int:
+    L = lib()
+    o = fvif_default_options()
+    o.enhn_gain_limit = float(gain_limit)
+    o.skip_scale0 = 1 if skip_scale0 else 0
+    for s in range(4):
+        o.min_val[s] = float(min_val[s])
+    ctx = L.fvif_create_ex(int(w), int(h), int(bitdepth), float(kernelscale),
+                           float(sigma_nsq), ctypes.byref(o))
+    if not ctx:
+        raise FvifError(L.fvif_last_error(None), "fvif_create_ex")
+    return ctx
+
+
+def fvif_score_debug(ctx: int, ref, dist, w: int, h: int,
+                     bitdepth: int) -> np.ndarray:
+    """Device inputs; the fifteen debug values per frame, shape (n, 15)."""
+    n = _frames(ref, w, h)
+    if _frames(dist, w, h) != n:
+        raise ValueError("ref and dist hold different frame counts")
+    out = np.zeros((n, 15), np.float64)
+    st = lib().fvif_score_debug(ctx, _dev_ptr(ref, bitdepth, "ref"),
+                                _dev_ptr(dist, bitdepth, "dist"), n,
+                                out.ctypes.data)
+    if st:
+        raise FvifError(st, "fvif_score_debug")
+    return out
 
 
 def fvif_destroy(ctx: int) -> None:
@@ -350,11 +402,18 @@ class Context:
     """Owning wrapper: ``with Context(w, h, bd, ks, nsq) as c: c.score(...)``."""
 
     def __init__(self, w: int, h: int, bitdepth: int, kernelscale: float = 1.0,
-                 sigma_nsq: float = 2.0):
+                 sigma_nsq: float = 2.0, gain_limit: float = 100.0,
+                 skip_scale0: bool = False, min_val=(0.0, 0.0, 0.0, 0.0)):
         self.w, self.h, self.bitdepth = int(w), int(h), int(bitdepth)
         self.kernelscale, self.sigma_nsq = float(kernelscale), float(sigma_nsq)
-        self.handle = fvif_create(self.w, self.h, self.bitdepth,
-                                  self.kernelscale, self.sigma_nsq)
+        self.handle = None
+        if gain_limit == 100.0 and not skip_scale0 and not any(min_val):
+            self.handle = fvif_create(self.w, self.h, self.bitdepth,
+                                      self.kernelscale, self.sigma_nsq)
+        else:
+            self.handle = fvif_create_ex(self.w, self.h, self.bitdepth,
+                                         self.kernelscale, self.sigma_nsq,
+                                         gain_limit, skip_scale0, min_val)
 
     def close(self) -> None:
         if self.handle:
@@ -378,6 +437,10 @@ class Context:
 
     def score(self, ref, dist) -> np.ndarray:
         return fvif_score(self.handle, ref, dist, self.w, self.h, self.bitdepth)
+
+    def score_debug(self, ref, dist) -> np.ndarray:
+        return fvif_score_debug(self.handle, ref, dist, self.w, self.h,
+                                self.bitdepth)
 
     def score_async(self, ref, dist, out) -> None:
         fvif_score_async(self.handle, ref, dist, out, self.w, self.h,

@@ -120,6 +120,8 @@ struct fvif_ctx {
     float kernelscale = 1.0f;
     double nsq = 2.0;
     float gain_limit = 100.0f;
+    int skip_scale0 = 0;
+    double min_val[kScales] = {0.0, 0.0, 0.0, 0.0};
     TermParams terms;
     int ws[kScales] = {}, hs[kScales] = {};
     Taps taps[kScales];
@@ -145,6 +147,10 @@ struct fvif_ctx {
     double *d_out = nullptr;     /* results of the synchronous calls      */
     double *h_out = nullptr;     /* pinned staging of d_out               */
     int out_cap = 0;
+    float2 *d_sums = nullptr;    /* per-(frame, scale) sums (debug)       */
+    double *d_debug = nullptr;   /* fifteen debug values per frame        */
+    double *h_debug = nullptr;   /* pinned staging of d_debug             */
+    int debug_cap = 0;
 
     /* opt-in launch timing: event pairs per kernel kind */
     bool profiling = false;
@@ -201,6 +207,12 @@ void release(fvif_ctx *c)
         cudaFree(c->d_out);
     if (c->h_out)
         cudaFreeHost(c->h_out);
+    if (c->d_sums)
+        cudaFree(c->d_sums);
+    if (c->d_debug)
+        cudaFree(c->d_debug);
+    if (c->h_debug)
+        cudaFreeHost(c->h_debug);
     for (int i = 0; i < 2; ++i) {
         if (c->stage[i])
             cudaFree(c->stage[i]);
@@ -292,6 +304,8 @@ int run_chunk(fvif_ctx *c, fvif_ctx::Lane &l, const void *ref,
             e = prof_end(c, FVIF_K_DECIMATE, st);
     }
     for (int s = 0; s < kScales && e == cudaSuccess; ++s) {
+        if (s == 0 && c->skip_scale0)
+            continue;
         StatsArgs a;
         a.src = (s == 0) ? s0 : pyr_src(c, l, s);
         a.w = c->ws[s];
@@ -319,6 +333,9 @@ int run_chunk(fvif_ctx *c, fvif_ctx::Lane &l, const void *ref,
         f.nframes = nf;
         f.out = out;
         f.sums = sums;
+        f.skip_scale0 = c->skip_scale0;
+        for (int s = 0; s < kScales; ++s)
+            f.min_val[s] = c->min_val[s];
         e = prof_begin(c, FVIF_K_FINAL, st);
         if (e == cudaSuccess)
             e = launch_final(f, st);
@@ -350,7 +367,7 @@ cudaError_t join_lanes(fvif_ctx *c)
 }
 
 int enqueue_all(fvif_ctx *c, const void *ref, const void *dist, int n,
-                double *out)
+                double *out, float2 *sums = nullptr)
 {
     const size_t fb = c->frame_bytes();
     int st = cuda_status(fork_lanes(c));
@@ -360,7 +377,8 @@ int enqueue_all(fvif_ctx *c, const void *ref, const void *dist, int n,
         st = run_chunk(c, c->lanes[i % kLanes],
                        static_cast<const unsigned char *>(ref) + fb * f0,
                        static_cast<const unsigned char *>(dist) + fb * f0, nf,
-                       out + (size_t)kScales * f0, nullptr);
+                       out + (size_t)kScales * f0,
+                       sums ? sums + (size_t)kScales * f0 : nullptr);
     }
     const int sj = cuda_status(join_lanes(c));
     return st != FVIF_OK ? st : sj;
@@ -388,6 +406,40 @@ int ensure_out(fvif_ctx *c, int n)
     c->d_out = d;
     c->h_out = h;
     c->out_cap = cap;
+    return FVIF_OK;
+}
+
+int ensure_debug(fvif_ctx *c, int n)
+{
+    if (n <= c->debug_cap)
+        return FVIF_OK;
+    int cap = c->debug_cap ? c->debug_cap : 64;
+    while (cap < n)
+        cap *= 2;
+    float2 *sm = nullptr;
+    double *d = nullptr, *h = nullptr;
+    cudaError_t e = cudaMalloc(&sm, sizeof(float2) * kScales * (size_t)cap);
+    if (e == cudaSuccess)
+        e = cudaMalloc(&d, sizeof(double) * 15 * (size_t)cap);
+    if (e == cudaSuccess)
+        e = cudaMallocHost(&h, sizeof(double) * 15 * (size_t)cap);
+    if (e != cudaSuccess) {
+        if (sm)
+            cudaFree(sm);
+        if (d)
+            cudaFree(d);
+        return FVIF_ENOMEM;
+    }
+    if (c->d_sums)
+        cudaFree(c->d_sums);
+    if (c->d_debug)
+        cudaFree(c->d_debug);
+    if (c->h_debug)
+        cudaFreeHost(c->h_debug);
+    c->d_sums = sm;
+    c->d_debug = d;
+    c->h_debug = h;
+    c->debug_cap = cap;
     return FVIF_OK;
 }
 
@@ -427,10 +479,35 @@ int ensure_pipeline(fvif_ctx *c)
 
 extern "C" {
 
+void fvif_default_options(fvif_options *opt)
+{
+    if (!opt)
+        return;
+    opt->enhn_gain_limit = 100.0f;
+    opt->skip_scale0 = 0;
+    for (int s = 0; s < kScales; ++s)
+        opt->min_val[s] = 0.0;
+}
+
 fvif_ctx *fvif_create(int w, int h, int bitdepth, float kernelscale,
                       double sigma_nsq)
 {
+    return fvif_create_ex(w, h, bitdepth, kernelscale, sigma_nsq, nullptr);
+}
+
+fvif_ctx *fvif_create_ex(int w, int h, int bitdepth, float kernelscale,
+                         double sigma_nsq, const fvif_options *opt)
+{
     g_create_status = FVIF_EINVAL;
+    fvif_options o;
+    fvif_default_options(&o);
+    if (opt)
+        o = *opt;
+    if (!(o.enhn_gain_limit > 0.0f) || !std::isfinite(o.enhn_gain_limit))
+        return nullptr;
+    for (int s = 0; s < kScales; ++s)
+        if (!std::isfinite(o.min_val[s]))
+            return nullptr;
     if (w < 16 || h < 16 || w > 16384 || h > 16384)
         return nullptr;
     if (bitdepth < 8 || bitdepth > 16)
@@ -450,6 +527,10 @@ fvif_ctx *fvif_create(int w, int h, int bitdepth, float kernelscale,
     c->bitdepth = bitdepth;
     c->kernelscale = kernelscale;
     c->nsq = sigma_nsq;
+    c->gain_limit = o.enhn_gain_limit;
+    c->skip_scale0 = o.skip_scale0 ? 1 : 0;
+    for (int s = 1; s < kScales; ++s)
+        c->min_val[s] = o.min_val[s];
     {
         const char *mode = std::getenv("FVIF_TERMS");
         const int m = (mode && std::strcmp(mode, "fp64") == 0) ? kTermsFp64
@@ -632,6 +713,40 @@ int fvif_score(fvif_ctx *ctx, const void *ref, const void *dist, int n_frames,
         st = enqueue_all(ctx, ref, dist, n_frames, ctx->d_out);
     if (st == FVIF_OK)
         st = finish_to_host(ctx, n_frames, out);
+    return set_status(ctx, st);
+}
+
+int fvif_score_debug(fvif_ctx *ctx, const void *ref, const void *dist,
+                     int n_frames, double *out)
+{
+    if (!ctx)
+        return FVIF_EINVAL;
+    if (n_frames < 0 || (n_frames > 0 && (!ref || !dist || !out)))
+        return set_status(ctx, FVIF_EINVAL);
+    if (n_frames == 0)
+        return set_status(ctx, FVIF_OK);
+    DeviceGuard g(ctx->device);
+    if (!g.ok)
+        return set_status(ctx, FVIF_ECUDA);
+    int st = ensure_out(ctx, n_frames);
+    if (st == FVIF_OK)
+        st = ensure_debug(ctx, n_frames);
+    if (st == FVIF_OK)
+        st = enqueue_all(ctx, ref, dist, n_frames, ctx->d_out, ctx->d_sums);
+    if (st == FVIF_OK)
+        st = cuda_status(launch_debug(ctx->d_out, ctx->d_sums, n_frames,
+                                      ctx->d_debug, ctx->stream));
+    cudaError_t e = cudaSuccess;
+    if (st == FVIF_OK)
+        e = cudaMemcpyAsync(ctx->h_debug, ctx->d_debug,
+                            sizeof(double) * 15 * (size_t)n_frames,
+                            cudaMemcpyDeviceToHost, ctx->stream);
+    if (st == FVIF_OK && e == cudaSuccess)
+        e = cudaStreamSynchronize(ctx->stream);
+    if (st == FVIF_OK && e != cudaSuccess)
+        st = cuda_status(e);
+    if (st == FVIF_OK)
+        std::memcpy(out, ctx->h_debug, sizeof(double) * 15 * (size_t)n_frames);
     return set_status(ctx, st);
 }
 

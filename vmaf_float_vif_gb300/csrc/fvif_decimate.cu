@@ -88,7 +88,8 @@ __global__ void __launch_bounds__(32 * kFinalWarps)
     if (warp >= a.nframes * kScales)
         return;
     const int f = warp / kScales, s = warp % kScales;
-    const int h = a.h[s];
+    const bool skipped = (s == 0 && a.skip_scale0);
+    const int h = skipped ? 0 : a.h[s];
     const float2 *r = a.rows + (size_t)f * a.rows_stride + a.rows_base[s];
     float num = 0.0f, den = 0.0f;
     for (int b = 0; b < h; b += kFinalBatch) {
@@ -107,10 +108,45 @@ __global__ void __launch_bounds__(32 * kFinalWarps)
         __syncwarp();
     }
     if (lane == 0) {
-        a.out[(size_t)f * kScales + s] = __ddiv_rn((double)num, (double)den);
+        double score = skipped ? 0.0 : __ddiv_rn((double)num, (double)den);
+        if (s > 0 && score < a.min_val[s])
+            score = a.min_val[s];
+        a.out[(size_t)f * kScales + s] = score;
         if (a.sums)
             a.sums[(size_t)f * kScales + s] = make_float2(num, den);
     }
+}
+
+/* One thread per frame: the fifteen debug values (see fvif_score_debug). */
+__global__ void debug_kernel(const double *scores, const float2 *sums, int n,
+                             double *out15)
+{
+    const int f = blockIdx.x * blockDim.x + threadIdx.x;
+    if (f >= n)
+        return;
+    const float2 *sm = sums + (size_t)f * kScales;
+    double *o = out15 + (size_t)f * 15;
+    double num = 0.0, den = 0.0;
+    for (int s = 0; s < kScales; ++s) {
+        num = __dadd_rn(num, (double)sm[s].x);
+        den = __dadd_rn(den, (double)sm[s].y);
+    }
+    for (int s = 0; s < kScales; ++s)
+        o[s] = scores[(size_t)f * kScales + s];
+    o[4] = __ddiv_rn(num, den);
+    o[5] = num;
+    o[6] = den;
+    for (int s = 0; s < kScales; ++s) {
+        o[7 + s] = (double)sm[s].x;
+        o[11 + s] = (double)sm[s].y;
+    }
+}
+
+cudaError_t launch_debug(const double *scores, const float2 *sums, int n,
+                         double *out15, cudaStream_t st)
+{
+    debug_kernel<<<(n + 127) / 128, 128, 0, st>>>(scores, sums, n, out15);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_final(const FinalArgs &a, cudaStream_t st)

@@ -81,6 +81,8 @@ struct FinalArgs {
     int nframes;
     double *out;       /* device, 4 per frame                               */
     float2 *sums;      /* optional device (num, den) per (frame, scale)     */
+    int skip_scale0;   /* scale 0 not computed: its sums and score are 0    */
+    double min_val[kScales]; /* floors on scales 1..3                       */
 };
 
 /* Taps of scale s for a kernelscale (host); FVIF_OK or FVIF_EINVAL. */
@@ -101,6 +103,9 @@ cudaError_t launch_stats(const StatsArgs &a, const Taps &taps,
 cudaError_t launch_decimate(const DecArgs &a, const Taps &taps,
                             cudaStream_t st);
 cudaError_t launch_final(const FinalArgs &a, cudaStream_t st);
+/* The fifteen debug outputs of n frames from their scores and sums. */
+cudaError_t launch_debug(const double *scores, const float2 *sums, int n,
+                         double *out15, cudaStream_t st);
 cudaError_t launch_unpack_planes(const SrcDesc &src, int w, int h,
                                  float *ref_out, float *dist_out,
                                  cudaStream_t st);

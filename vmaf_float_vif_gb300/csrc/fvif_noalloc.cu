@@ -179,7 +179,7 @@ extern "C" int fvif_score_noalloc(int w, int h, int bitdepth,
             e = launch_stats(a, taps[s], stream);
         }
         if (e == cudaSuccess) {
-            FinalArgs fa;
+            FinalArgs fa = {};
             fa.rows = rows;
             fa.rows_stride = rows_total;
             for (int s = 0; s < kScales; ++s) {
