@@ -74,6 +74,7 @@ void make_term_params(double nsq, float gain_limit, int mode, TermParams &t)
     std::memset(&t, 0, sizeof t);
     t.nsq = nsq;
     t.gain_limit = gain_limit;
+    t.one2 = make_float2(1.0f, 1.0f);
     float up = (float)nsq;
     if ((double)up < nsq)
         up = std::nextafter(up, INFINITY);

@@ -49,6 +49,7 @@ struct TermParams {
     float n_hi, n_lo; /* nsq = n_hi + n_lo + e, |e| <= 2^-48 nsq            */
     float rcp_n;      /* fl32(1 / n_hi)                                     */
     float inv_pow2;   /* 1 / nsq when nsq is a power of two, else 0         */
+    float2 one2;      /* (1, 1), read at run time by the packed sums        */
     int mode;         /* TermsMode                                          */
 };
 
