@@ -73,11 +73,20 @@ fvif_ctx *fvif_create(int w, int h, int bitdepth, float kernelscale,
  *  skip_scale0     : nonzero -> scale 0 contributes nothing: its sums and
  *                    vif_scale0 are 0 (default 0).
  *  min_val[s]      : for s = 1..3, vif_scale_s = max(vif_scale_s, min_val[s])
- *                    (defaults 0; min_val[0] is ignored). */
+ *                    (defaults 0; min_val[0] is ignored).
+ *  frame_stride    : samples from the start of one input frame to the start
+ *                    of the next (0 = w*h, planes packed back to back).  With
+ *                    planar YUV frames (4:2:0, 4:2:2, 4:4:4) the luma plane
+ *                    comes first, so the stride of the whole frame lets the
+ *                    library read the luma planes in place: w*h*3/2, w*h*2
+ *                    or w*h*3.  Must be 0 or >= w*h.  Applies to every
+ *                    scoring entry point of the context; fvif_score_host
+ *                    copies only the luma planes to the device. */
 typedef struct fvif_options {
     float enhn_gain_limit;
     int skip_scale0;
     double min_val[4];
+    long long frame_stride;
 } fvif_options;
 
 /* Fill *opt with the defaults above. */
@@ -89,7 +98,8 @@ fvif_ctx *fvif_create_ex(int w, int h, int bitdepth, float kernelscale,
                          double sigma_nsq, const fvif_options *opt);
 
 /* Score n_frames frame pairs whose samples are in DEVICE memory (caller
- * owned, readable for the whole call).  out: HOST memory of 4*n_frames
+ * owned, readable for the whole call; frames frame_stride samples apart,
+ * see fvif_options).  out: HOST memory of 4*n_frames
  * doubles.  Synchronous: returns after out is written.  n_frames == 0 is a
  * no-op.  Frames are processed in chunks; no host round trip inside a
  * chunk. */

@@ -270,3 +270,31 @@ def test_debug_outputs_default_options(fv):
     for f in range(case.frames):
         _, want = oracle.frame_opts(ref[f], dist[f], 8, 1.0, 2.0)
         assert_bitwise(dbg[f], want, "debug c1 f%d" % f)
+
+
+@pytest.mark.parametrize("factor", [1.5, 2.0, 3.0], ids=["420", "422", "444"])
+@pytest.mark.parametrize("bd", [8, 10])
+def test_planar_yuv_frames(fv, factor, bd):
+    """Frames whose luma planes are followed by chroma planes: with
+    frame_stride the library reads the luma planes in place (device input)
+    or copies only them (host input); chroma never enters the score."""
+    case = S.custom_noise_case(200, 120, bd, frames=5)
+    ref, dist = case.batch(range(case.frames))
+    w, h, n = case.w, case.h, case.frames
+    stride = int(w * h * factor)
+    rng = np.random.default_rng(11)
+
+    def pack(planes):
+        buf = rng.integers(0, 1 << bd, size=n * stride).astype(case.dtype)
+        for k in range(n):
+            buf[k * stride:k * stride + w * h] = planes[k].ravel()
+        return buf
+
+    rbuf, dbuf = pack(ref), pack(dist)
+    want = oracle_scores(ref, dist, bd, 1.0, 2.0)
+    with fv.Context(w, h, bd, 1.0, 2.0, frame_stride=stride) as ctx:
+        assert_bitwise(ctx.score(to_device(rbuf), to_device(dbuf)), want,
+                       "device %s" % factor)
+        assert_bitwise(ctx.score_host(rbuf, dbuf), want, "host %s" % factor)
+        assert_bitwise(ctx.score_debug(to_device(rbuf), to_device(dbuf))[:, :4],
+                       want, "debug %s" % factor)

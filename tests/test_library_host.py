@@ -102,3 +102,18 @@ def test_create_ex_rejects_invalid_options(L, field, value):
         setattr(o, field, value)
     assert not L.fvif_create_ex(64, 64, 8, 1.0, 2.0, ctypes.byref(o))
     assert L.fvif_last_error(None) == fv.FVIF_EINVAL
+
+
+def test_create_ex_rejects_short_frame_stride(L):
+    o = _lib.fvif_default_options()
+    o.frame_stride = 64 * 64 - 1
+    assert not L.fvif_create_ex(64, 64, 8, 1.0, 2.0, ctypes.byref(o))
+    assert L.fvif_last_error(None) == fv.FVIF_EINVAL
+
+
+def test_frame_count_with_stride():
+    import numpy as np
+    a = np.zeros(3 * 96, np.uint8)
+    assert _lib._frames(a, 8, 8, 96) == 3
+    with pytest.raises(ValueError):
+        _lib._frames(a, 8, 8, 100)

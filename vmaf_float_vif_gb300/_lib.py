@@ -37,7 +37,8 @@ class FvifOptions(ctypes.Structure):
     """Mirror of struct fvif_options."""
     _fields_ = [("enhn_gain_limit", ctypes.c_float),
                 ("skip_scale0", ctypes.c_int),
-                ("min_val", ctypes.c_double * 4)]
+                ("min_val", ctypes.c_double * 4),
+                ("frame_stride", ctypes.c_longlong)]
 
 FVIF_K_DECIMATE, FVIF_K_STATS0, FVIF_K_STATS123, FVIF_K_FINAL = range(4)
 KERNEL_KINDS = {"decimate": 0, "stats_scale0": 1, "stats_scale123": 2,
@@ -156,11 +157,14 @@ def _host_array(a, bitdepth: int, what: str) -> np.ndarray:
     return a
 
 
-def _frames(a, w: int, h: int) -> int:
+def _frames(a, w: int, h: int, stride: int = 0) -> int:
+    """Frames in a buffer of frames `stride` samples apart (0: w*h)."""
     n_elems = int(np.prod(a.shape)) if len(a.shape) else 0
-    if n_elems % (w * h):
-        raise ValueError("buffer is not a whole number of %dx%d frames" % (w, h))
-    return n_elems // (w * h)
+    step = stride or w * h
+    if n_elems % step:
+        raise ValueError("buffer is not a whole number of frames of %d "
+                         "samples" % step)
+    return n_elems // step
 
 
 # ---------------------------------------------------------------------------
@@ -186,13 +190,14 @@ def fvif_default_options() -> FvifOptions:
 def fvif_create_ex(w: int, h: int, bitdepth: int, kernelscale: float,
                    sigma_nsq: float, gain_limit: float = 100.0,
                    skip_scale0: bool = False,
-                   min_val=(0.0, 0.0, 0.0, 0.0)) -> int:
+                   min_val=(0.0, 0.0, 0.0, 0.0), frame_stride: int = 0) -> int:
     L = lib()
     o = fvif_default_options()
     o.enhn_gain_limit = float(gain_limit)
     o.skip_scale0 = 1 if skip_scale0 else 0
     for s in range(4):
         o.min_val[s] = float(min_val[s])
+    o.frame_stride = int(frame_stride)
     ctx = L.fvif_create_ex(int(w), int(h), int(bitdepth), float(kernelscale),
                            float(sigma_nsq), ctypes.byref(o))
     if not ctx:
@@ -201,10 +206,10 @@ def fvif_create_ex(w: int, h: int, bitdepth: int, kernelscale: float,
 
 
 def fvif_score_debug(ctx: int, ref, dist, w: int, h: int,
-                     bitdepth: int) -> np.ndarray:
+                     bitdepth: int, stride: int = 0) -> np.ndarray:
     """Device inputs; the fifteen debug values per frame, shape (n, 15)."""
-    n = _frames(ref, w, h)
-    if _frames(dist, w, h) != n:
+    n = _frames(ref, w, h, stride)
+    if _frames(dist, w, h, stride) != n:
         raise ValueError("ref and dist hold different frame counts")
     out = np.zeros((n, 15), np.float64)
     st = lib().fvif_score_debug(ctx, _dev_ptr(ref, bitdepth, "ref"),
@@ -248,10 +253,11 @@ def fvif_get_taps(ctx: int, scale: int) -> np.ndarray:
     return buf[:n].copy()
 
 
-def fvif_score(ctx: int, ref, dist, w: int, h: int, bitdepth: int) -> np.ndarray:
+def fvif_score(ctx: int, ref, dist, w: int, h: int, bitdepth: int,
+               stride: int = 0) -> np.ndarray:
     """Device inputs (CUDA tensors), host results of shape (n, 4)."""
-    n = _frames(ref, w, h)
-    if _frames(dist, w, h) != n:
+    n = _frames(ref, w, h, stride)
+    if _frames(dist, w, h, stride) != n:
         raise ValueError("ref and dist hold different frame counts")
     out = np.zeros((n, 4), np.float64)
     st = lib().fvif_score(ctx, _dev_ptr(ref, bitdepth, "ref"),
@@ -263,11 +269,11 @@ def fvif_score(ctx: int, ref, dist, w: int, h: int, bitdepth: int) -> np.ndarray
 
 
 def fvif_score_async(ctx: int, ref, dist, out, w: int, h: int,
-                     bitdepth: int) -> None:
+                     bitdepth: int, stride: int = 0) -> None:
     """Device inputs and a device float64 output of 4*n values; enqueues only."""
     import torch
-    n = _frames(ref, w, h)
-    if _frames(dist, w, h) != n:
+    n = _frames(ref, w, h, stride)
+    if _frames(dist, w, h, stride) != n:
         raise ValueError("ref and dist hold different frame counts")
     if (not isinstance(out, torch.Tensor) or not out.is_cuda or
             out.dtype != torch.float64 or out.numel() < 4 * n or
@@ -282,13 +288,13 @@ def fvif_score_async(ctx: int, ref, dist, out, w: int, h: int,
 
 
 def fvif_score_host(ctx: int, ref, dist, w: int, h: int,
-                    bitdepth: int) -> np.ndarray:
+                    bitdepth: int, stride: int = 0) -> np.ndarray:
     """Host inputs (numpy arrays or CPU tensors, ideally page-locked), host
     results of shape (n, 4)."""
     r = _host_array(ref, bitdepth, "ref")
     d = _host_array(dist, bitdepth, "dist")
-    n = _frames(r, w, h)
-    if _frames(d, w, h) != n:
+    n = _frames(r, w, h, stride)
+    if _frames(d, w, h, stride) != n:
         raise ValueError("ref and dist hold different frame counts")
     out = np.zeros((n, 4), np.float64)
     st = lib().fvif_score_host(ctx, r.ctypes.data, d.ctypes.data, n,
@@ -403,17 +409,21 @@ class Context:
 
     def __init__(self, w: int, h: int, bitdepth: int, kernelscale: float = 1.0,
                  sigma_nsq: float = 2.0, gain_limit: float = 100.0,
-                 skip_scale0: bool = False, min_val=(0.0, 0.0, 0.0, 0.0)):
+                 skip_scale0: bool = False, min_val=(0.0, 0.0, 0.0, 0.0),
+                 frame_stride: int = 0):
         self.w, self.h, self.bitdepth = int(w), int(h), int(bitdepth)
         self.kernelscale, self.sigma_nsq = float(kernelscale), float(sigma_nsq)
+        self.stride = int(frame_stride)
         self.handle = None
-        if gain_limit == 100.0 and not skip_scale0 and not any(min_val):
+        if (gain_limit == 100.0 and not skip_scale0 and not any(min_val)
+                and not frame_stride):
             self.handle = fvif_create(self.w, self.h, self.bitdepth,
                                       self.kernelscale, self.sigma_nsq)
         else:
             self.handle = fvif_create_ex(self.w, self.h, self.bitdepth,
                                          self.kernelscale, self.sigma_nsq,
-                                         gain_limit, skip_scale0, min_val)
+                                         gain_limit, skip_scale0, min_val,
+                                         frame_stride)
 
     def close(self) -> None:
         if self.handle:
@@ -436,19 +446,20 @@ class Context:
         fvif_set_stream(self.handle, stream)
 
     def score(self, ref, dist) -> np.ndarray:
-        return fvif_score(self.handle, ref, dist, self.w, self.h, self.bitdepth)
+        return fvif_score(self.handle, ref, dist, self.w, self.h, self.bitdepth,
+                          self.stride)
 
     def score_debug(self, ref, dist) -> np.ndarray:
         return fvif_score_debug(self.handle, ref, dist, self.w, self.h,
-                                self.bitdepth)
+                                self.bitdepth, self.stride)
 
     def score_async(self, ref, dist, out) -> None:
         fvif_score_async(self.handle, ref, dist, out, self.w, self.h,
-                         self.bitdepth)
+                         self.bitdepth, self.stride)
 
     def score_host(self, ref, dist) -> np.ndarray:
         return fvif_score_host(self.handle, ref, dist, self.w, self.h,
-                               self.bitdepth)
+                               self.bitdepth, self.stride)
 
     def taps(self, scale: int) -> np.ndarray:
         return fvif_get_taps(self.handle, scale)

@@ -166,7 +166,9 @@ struct fvif_ctx {
     cudaEvent_t consumed[2] = {};
 
     size_t sample_bytes() const { return bitdepth == 8 ? 1u : 2u; }
-    size_t frame_bytes() const { return (size_t)w * h * sample_bytes(); }
+    size_t frame_stride = 0; /* samples between consecutive input frames */
+    size_t plane_bytes() const { return (size_t)w * h * sample_bytes(); }
+    size_t frame_bytes() const { return frame_stride * sample_bytes(); }
 };
 
 namespace {
@@ -258,7 +260,8 @@ cudaError_t prof_end(fvif_ctx *c, int k, cudaStream_t st)
     return e;
 }
 
-SrcDesc scale0_src(const fvif_ctx *c, const void *ref, const void *dist)
+SrcDesc scale0_src(const fvif_ctx *c, const void *ref, const void *dist,
+                   size_t frame_elems)
 {
     SrcDesc d;
     d.kind = c->bitdepth == 8 ? SrcKind::U8 : SrcKind::U16;
@@ -266,7 +269,7 @@ SrcDesc scale0_src(const fvif_ctx *c, const void *ref, const void *dist)
     d.y = dist;
     d.scale = c->bitdepth == 8 ? 1.0f
                                : std::ldexp(1.0f, -(c->bitdepth - 8));
-    d.frame_elems = (size_t)c->w * c->h;
+    d.frame_elems = frame_elems;
     return d;
 }
 
@@ -284,10 +287,11 @@ SrcDesc pyr_src(const fvif_ctx *c, const fvif_ctx::Lane &l, int s)
 /* One chunk (nf <= chunk frames) on the context stream: the pyramid, the
  * four statistic launches and the final reduction into out (device). */
 int run_chunk(fvif_ctx *c, fvif_ctx::Lane &l, const void *ref,
-              const void *dist, int nf, double *out, float2 *sums)
+              const void *dist, int nf, double *out, float2 *sums,
+              size_t in_frame_elems)
 {
     cudaStream_t st = l.stream;
-    const SrcDesc s0 = scale0_src(c, ref, dist);
+    const SrcDesc s0 = scale0_src(c, ref, dist, in_frame_elems);
     cudaError_t e = cudaSuccess;
 
     for (int s = 1; s < kScales && e == cudaSuccess; ++s) {
@@ -379,7 +383,8 @@ int enqueue_all(fvif_ctx *c, const void *ref, const void *dist, int n,
                        static_cast<const unsigned char *>(ref) + fb * f0,
                        static_cast<const unsigned char *>(dist) + fb * f0, nf,
                        out + (size_t)kScales * f0,
-                       sums ? sums + (size_t)kScales * f0 : nullptr);
+                       sums ? sums + (size_t)kScales * f0 : nullptr,
+                       c->frame_stride);
     }
     const int sj = cuda_status(join_lanes(c));
     return st != FVIF_OK ? st : sj;
@@ -461,7 +466,7 @@ int ensure_pipeline(fvif_ctx *c)
 {
     if (c->copy_stream)
         return FVIF_OK;
-    const size_t slot = 2 * c->frame_bytes() * (size_t)c->chunk;
+    const size_t slot = 2 * c->plane_bytes() * (size_t)c->chunk;
     cudaError_t e = cudaStreamCreateWithFlags(&c->copy_stream,
                                               cudaStreamNonBlocking);
     for (int i = 0; i < 2 && e == cudaSuccess; ++i) {
@@ -486,6 +491,7 @@ void fvif_default_options(fvif_options *opt)
         return;
     opt->enhn_gain_limit = 100.0f;
     opt->skip_scale0 = 0;
+    opt->frame_stride = 0;
     for (int s = 0; s < kScales; ++s)
         opt->min_val[s] = 0.0;
 }
@@ -509,6 +515,8 @@ fvif_ctx *fvif_create_ex(int w, int h, int bitdepth, float kernelscale,
     for (int s = 0; s < kScales; ++s)
         if (!std::isfinite(o.min_val[s]))
             return nullptr;
+    if (o.frame_stride != 0 && o.frame_stride < (long long)w * h)
+        return nullptr;
     if (w < 16 || h < 16 || w > 16384 || h > 16384)
         return nullptr;
     if (bitdepth < 8 || bitdepth > 16)
@@ -528,6 +536,8 @@ fvif_ctx *fvif_create_ex(int w, int h, int bitdepth, float kernelscale,
     c->bitdepth = bitdepth;
     c->kernelscale = kernelscale;
     c->nsq = sigma_nsq;
+    c->frame_stride = o.frame_stride ? (size_t)o.frame_stride
+                                     : (size_t)w * (size_t)h;
     c->gain_limit = o.enhn_gain_limit;
     c->skip_scale0 = o.skip_scale0 ? 1 : 0;
     for (int s = 1; s < kScales; ++s)
@@ -769,8 +779,11 @@ int fvif_score_host(fvif_ctx *ctx, const void *ref, const void *dist,
     if (st != FVIF_OK)
         return set_status(ctx, st);
 
+    /* the staging slots hold the luma planes packed (w*h samples apart);
+     * the host frames may be further apart (frame_stride) */
     const size_t fb = ctx->frame_bytes();
-    const size_t half = fb * (size_t)ctx->chunk;
+    const size_t pb = ctx->plane_bytes();
+    const size_t half = pb * (size_t)ctx->chunk;
     cudaError_t e = fork_lanes(ctx);
     int i = 0;
     for (int f0 = 0; f0 < n_frames && e == cudaSuccess; f0 += ctx->chunk, ++i) {
@@ -784,17 +797,17 @@ int fvif_score_host(fvif_ctx *ctx, const void *ref, const void *dist,
         /* the slot is free once the chunk that used it two steps ago ran */
         e = cudaStreamWaitEvent(ctx->copy_stream, ctx->consumed[slot], 0);
         if (e == cudaSuccess)
-            e = cudaMemcpyAsync(dref,
-                                static_cast<const unsigned char *>(ref) +
-                                    fb * f0,
-                                fb * nf, cudaMemcpyHostToDevice,
-                                ctx->copy_stream);
+            e = cudaMemcpy2DAsync(dref, pb,
+                                  static_cast<const unsigned char *>(ref) +
+                                      fb * f0,
+                                  fb, pb, nf, cudaMemcpyHostToDevice,
+                                  ctx->copy_stream);
         if (e == cudaSuccess)
-            e = cudaMemcpyAsync(ddist,
-                                static_cast<const unsigned char *>(dist) +
-                                    fb * f0,
-                                fb * nf, cudaMemcpyHostToDevice,
-                                ctx->copy_stream);
+            e = cudaMemcpy2DAsync(ddist, pb,
+                                  static_cast<const unsigned char *>(dist) +
+                                      fb * f0,
+                                  fb, pb, nf, cudaMemcpyHostToDevice,
+                                  ctx->copy_stream);
         if (e == cudaSuccess)
             e = cudaEventRecord(ctx->copied[slot], ctx->copy_stream);
         if (e == cudaSuccess)
@@ -802,7 +815,8 @@ int fvif_score_host(fvif_ctx *ctx, const void *ref, const void *dist,
         if (e != cudaSuccess)
             break;
         st = run_chunk(ctx, lane, dref, ddist, nf,
-                       ctx->d_out + (size_t)kScales * f0, nullptr);
+                       ctx->d_out + (size_t)kScales * f0, nullptr,
+                       (size_t)ctx->w * ctx->h);
         if (st != FVIF_OK)
             break;
         e = cudaEventRecord(ctx->consumed[slot], lane.stream);
@@ -850,7 +864,8 @@ int fvif_debug_frame(fvif_ctx *ctx, const void *ref, const void *dist,
     fvif_ctx::Lane &lane = ctx->lanes[0];
     int st = cuda_status(fork_lanes(ctx));
     if (st == FVIF_OK)
-        st = run_chunk(ctx, lane, ref, dist, 1, ctx->d_out, ctx->sums);
+        st = run_chunk(ctx, lane, ref, dist, 1, ctx->d_out, ctx->sums,
+                       (size_t)ctx->w * ctx->h);
     const int sj = cuda_status(join_lanes(ctx));
     if (st == FVIF_OK)
         st = sj;
@@ -866,8 +881,9 @@ int fvif_debug_frame(fvif_ctx *ctx, const void *ref, const void *dist,
         size_t off = 0;
         for (int s = 0; s < kScales && e == cudaSuccess; ++s) {
             const size_t np = (size_t)ctx->ws[s] * ctx->hs[s];
-            const SrcDesc d = s == 0 ? scale0_src(ctx, ref, dist)
-                                     : pyr_src(ctx, lane, s);
+            const SrcDesc d =
+                s == 0 ? scale0_src(ctx, ref, dist, (size_t)ctx->w * ctx->h)
+                       : pyr_src(ctx, lane, s);
             e = launch_unpack_planes(d, ctx->ws[s], ctx->hs[s], tmp + off,
                                      tmp + off + np, ctx->stream);
             off += 2 * np;
