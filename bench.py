@@ -216,6 +216,28 @@ def load_traffic(workload):
     return t.get("per_launch_bytes", {}).get(workload)
 
 
+def host_link_gbs() -> float:
+    """Host-to-device bandwidth of this process's GPU for page-locked
+    memory (1 GiB, best of 5 copies, CUDA events)."""
+    import torch
+    n = 1 << 30
+    h = torch.empty(n, dtype=torch.uint8).pin_memory()
+    d = torch.empty(n, dtype=torch.uint8, device="cuda")
+    d.copy_(h, non_blocking=True)
+    torch.cuda.synchronize()
+    best = 0.0
+    for _ in range(5):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        d.copy_(h, non_blocking=True)
+        e1.record()
+        torch.cuda.synchronize()
+        best = max(best, n / (e0.elapsed_time(e1) / 1e3) / 1e9)
+    del h, d
+    return best
+
+
 def stats_ops_per_pixel(ntaps: int) -> int:
     """Algorithmic fp32 operations of the statistic per pixel: five
     quantities, two passes, ntaps products and ntaps-1 sums each, plus the
@@ -321,6 +343,7 @@ def run_ours(args):
                               else dist_np).pin_memory()
         hr = pr.numpy().view(ref.dtype)
         hd = pd.numpy().view(dist_np.dtype)
+        link = host_link_gbs()
         ctx.set_stream(None)
         for _ in range(max(1, args.warmup)):
             ctx.score_host(hr, hd)
@@ -330,13 +353,17 @@ def run_ours(args):
         e_stop = torch.cuda.Event(enable_timing=True)
         t0 = time.perf_counter()
         e_start.record()
+        step_ms = []
         for _ in range(args.e2e_steps):
-            host_scores = ctx.score_host(hr, hd)
+            ts = time.perf_counter()
+            host_scores = ctx.score_host(hr, hd)   # returns after the d2h read
+            step_ms.append(1e3 * (time.perf_counter() - ts))
         e_stop.record()
         torch.cuda.synchronize()
         wall = time.perf_counter() - t0
         barrier()
         wall = max_over_ranks(wall, world)
+        link_after = host_link_gbs()
         if not np.array_equal(host_scores, scores):
             raise RuntimeError("fvif_score_host and fvif_score_async differ")
         e2e = {"value": job_throughput(frames, args.e2e_steps, world, wall),
@@ -344,7 +371,14 @@ def run_ours(args):
                "h2d_bytes_per_step": int(ref.nbytes + dist_np.nbytes),
                "d2h_bytes_per_step": int(scores.nbytes),
                "ms_per_step": 1e3 * wall / args.e2e_steps,
-               "api": "fvif_score_host (page-locked host inputs)"}
+               "api": "fvif_score_host (page-locked host inputs)",
+               "step_ms": [round(t, 2) for t in step_ms],
+               "h2d_link_gbs": [round(link, 1), round(link_after, 1)],
+               "link_floor_ms": 1e3 * (ref.nbytes + dist_np.nbytes) / 1e9 / link,
+               "link_note": "plain page-locked 1 GiB host-to-device copy, best "
+                            "of 5, measured in the same process just before and "
+                            "just after the e2e region; a step cannot finish "
+                            "faster than its input bytes over this link"}
 
     if rank != 0:
         ctx.close()

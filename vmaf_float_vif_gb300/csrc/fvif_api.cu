@@ -18,6 +18,7 @@ namespace {
 
 constexpr int kDefaultChunk = 16;
 constexpr int kLanes = 2; /* chunks alternate between two streams */
+constexpr int kMaxStage = 4; /* host-input staging slots, at most */
 
 thread_local int g_create_status = FVIF_OK;
 
@@ -160,10 +161,12 @@ struct fvif_ctx {
     long long launches[FVIF_K_COUNT] = {};
 
     /* host-input pipeline (allocated on first fvif_score_host) */
-    unsigned char *stage[2] = {};
+    int stage_slots = 3;        /* staging slots of the host path        */
+    int host_lanes = kLanes;    /* compute lanes the host path uses      */
+    unsigned char *stage[kMaxStage] = {};
     cudaStream_t copy_stream = nullptr;
-    cudaEvent_t copied[2] = {};
-    cudaEvent_t consumed[2] = {};
+    cudaEvent_t copied[kMaxStage] = {};
+    cudaEvent_t consumed[kMaxStage] = {};
 
     size_t sample_bytes() const { return bitdepth == 8 ? 1u : 2u; }
     size_t frame_stride = 0; /* samples between consecutive input frames */
@@ -216,7 +219,7 @@ void release(fvif_ctx *c)
         cudaFree(c->d_debug);
     if (c->h_debug)
         cudaFreeHost(c->h_debug);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kMaxStage; ++i) {
         if (c->stage[i])
             cudaFree(c->stage[i]);
         if (c->copied[i])
@@ -469,7 +472,7 @@ int ensure_pipeline(fvif_ctx *c)
     const size_t slot = 2 * c->plane_bytes() * (size_t)c->chunk;
     cudaError_t e = cudaStreamCreateWithFlags(&c->copy_stream,
                                               cudaStreamNonBlocking);
-    for (int i = 0; i < 2 && e == cudaSuccess; ++i) {
+    for (int i = 0; i < c->stage_slots && e == cudaSuccess; ++i) {
         e = cudaMalloc(&c->stage[i], slot);
         if (e == cudaSuccess)
             e = cudaEventCreateWithFlags(&c->copied[i],
@@ -560,6 +563,16 @@ fvif_ctx *fvif_create_ex(int w, int h, int bitdepth, float kernelscale,
         const int v = std::atoi(env);
         if (v > 0 && v <= 256)
             c->chunk = v;
+    }
+    if (const char *env = std::getenv("FVIF_HOST_SLOTS")) {
+        const int v = std::atoi(env);
+        if (v >= 2 && v <= kMaxStage)
+            c->stage_slots = v;
+    }
+    if (const char *env = std::getenv("FVIF_HOST_LANES")) {
+        const int v = std::atoi(env);
+        if (v >= 1 && v <= kLanes)
+            c->host_lanes = v;
     }
     cudaError_t e = cudaGetDevice(&c->device);
     int rows_total = 0;
@@ -789,12 +802,13 @@ int fvif_score_host(fvif_ctx *ctx, const void *ref, const void *dist,
     for (int f0 = 0; f0 < n_frames && e == cudaSuccess; f0 += ctx->chunk, ++i) {
         const int nf = (n_frames - f0 < ctx->chunk) ? n_frames - f0
                                                     : ctx->chunk;
-        /* staging slot i % 2 is scored on lane i % 2 */
-        const int slot = i % kLanes;
-        fvif_ctx::Lane &lane = ctx->lanes[slot];
+        /* chunk i is copied into staging slot i % slots while earlier
+         * chunks are scored, and scored on lane i % lanes */
+        const int slot = i % ctx->stage_slots;
+        fvif_ctx::Lane &lane = ctx->lanes[i % ctx->host_lanes];
         unsigned char *dref = ctx->stage[slot];
         unsigned char *ddist = ctx->stage[slot] + half;
-        /* the slot is free once the chunk that used it two steps ago ran */
+        /* the slot is free once the chunk that used it last was scored */
         e = cudaStreamWaitEvent(ctx->copy_stream, ctx->consumed[slot], 0);
         if (e == cudaSuccess)
             e = cudaMemcpy2DAsync(dref, pb,
