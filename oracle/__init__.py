@@ -24,6 +24,9 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "fvif_oracle.c")
 _HDR = os.path.join(_HERE, "fvif_oracle.h")
+_SSIM_SRC = os.path.join(_HERE, "fssim_oracle.c")
+_SSIM_HDR = os.path.join(_HERE, "fssim_oracle.h")
+_SOURCES = (_SRC, _SSIM_SRC)
 _OUT_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_OUT_DIR, "liboracle.so")
 
@@ -41,30 +44,43 @@ def build(force: bool = False) -> str:
     """Compile the oracle into ``oracle/_build/liboracle.so`` (gcc)."""
     os.makedirs(_OUT_DIR, exist_ok=True)
     stale = force or not os.path.exists(_LIB_PATH) or any(
-        os.path.getmtime(p) > os.path.getmtime(_LIB_PATH) for p in (_SRC, _HDR))
+        os.path.getmtime(p) > os.path.getmtime(_LIB_PATH)
+        for p in (*_SOURCES, _HDR, _SSIM_HDR))
     if stale:
         tmp = _LIB_PATH + ".tmp.%d" % os.getpid()
-        cmd = ["gcc", *CFLAGS, "-o", tmp, _SRC, "-lm"]
+        cmd = ["gcc", *CFLAGS, "-o", tmp, *_SOURCES, "-lm"]
         subprocess.run(cmd, check=True)
         os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
 
 
-def build_variant(source_text: str, tag: str) -> ctypes.CDLL:
-    """Compile an edited copy of the oracle source (used by tests that plant
-    a mistake in the oracle and check that a pin catches it)."""
+def build_variant(source_text: str, tag: str,
+                  ssim_source_text: str | None = None) -> ctypes.CDLL:
+    """Compile an edited copy of the oracle sources (used by tests that plant
+    a mistake in the oracle and check that a pin catches it).  The float VIF
+    source is ``source_text``; the float_ssim decimation source is
+    ``ssim_source_text``, or the committed one when None."""
     d = tempfile.mkdtemp(prefix="oracle_variant_")
     src = os.path.join(d, "variant_%s.c" % tag)
+    src2 = os.path.join(d, "variant_ssim_%s.c" % tag)
     so = os.path.join(d, "libvariant_%s.so" % tag)
     with open(src, "w") as f:
         f.write(source_text)
-    subprocess.run(["gcc", *CFLAGS, "-I", _HERE, "-o", so, src, "-lm"],
+    with open(src2, "w") as f:
+        f.write(ssim_source_text if ssim_source_text is not None
+                else ssim_source())
+    subprocess.run(["gcc", *CFLAGS, "-I", _HERE, "-o", so, src, src2, "-lm"],
                    check=True)
     return _declare(ctypes.CDLL(so))
 
 
 def source_text() -> str:
     with open(_SRC) as f:
+        return f.read()
+
+
+def ssim_source() -> str:
+    with open(_SSIM_SRC) as f:
         return f.read()
 
 
@@ -107,6 +123,23 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
         ctypes.c_int, ctypes.c_float, ctypes.c_double, ctypes.c_int, _f64p]
     lib.fvo_score.restype = ctypes.c_int
+    _ip = ctypes.POINTER(ctypes.c_int)
+    lib.fso_auto_scale.argtypes = [ctypes.c_int, ctypes.c_int]
+    lib.fso_auto_scale.restype = ctypes.c_int
+    lib.fso_mirror.argtypes = [ctypes.c_int, ctypes.c_int]
+    lib.fso_mirror.restype = ctypes.c_int
+    lib.fso_out_size.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                 _ip, _ip]
+    lib.fso_out_size.restype = ctypes.c_int
+    lib.fso_tap.argtypes = [ctypes.c_int]
+    lib.fso_tap.restype = ctypes.c_float
+    lib.fso_decimate_plane.argtypes = [_f32p, ctypes.c_int, ctypes.c_int,
+                                       ctypes.c_int, _f32p]
+    lib.fso_decimate_plane.restype = ctypes.c_int
+    lib.fso_decimate.argtypes = [
+        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
+        ctypes.c_int, ctypes.c_int, ctypes.c_int, _f32p, _f32p, _f32p]
+    lib.fso_decimate.restype = ctypes.c_int
     return lib
 
 
@@ -275,3 +308,73 @@ def score(ref: np.ndarray, dist: np.ndarray, bitdepth: int,
         for f, fu in enumerate(futs):
             out[f] = fu.result()
     return out
+
+
+# ---------------------------------------------------------------------------
+# float_ssim auto-scale decimation (fssim_oracle.c)
+
+
+def ssim_auto_scale(w: int, h: int, L=None) -> int:
+    return int((L or lib()).fso_auto_scale(w, h))
+
+
+def ssim_mirror(j: int, n: int, L=None) -> int:
+    return int((L or lib()).fso_mirror(j, n))
+
+
+def ssim_out_size(w: int, h: int, scale: int, L=None):
+    sw, sh = ctypes.c_int(), ctypes.c_int()
+    if (L or lib()).fso_out_size(w, h, scale, ctypes.byref(sw),
+                                 ctypes.byref(sh)):
+        raise ValueError("bad size or scale")
+    return sw.value, sh.value
+
+
+def ssim_tap(scale: int, L=None) -> np.float32:
+    return np.float32((L or lib()).fso_tap(scale))
+
+
+def ssim_decimate_plane(img: np.ndarray, scale: int, L=None) -> np.ndarray:
+    """One fp32 plane (h, w) decimated by ``scale``."""
+    L = L or lib()
+    img = np.ascontiguousarray(img, np.float32)
+    h, w = img.shape
+    sw, sh = ssim_out_size(w, h, scale, L)
+    out = np.zeros((sh, sw), np.float32)
+    if L.fso_decimate_plane(_fptr(img), w, h, scale, _fptr(out)):
+        raise ValueError("bad plane")
+    return out
+
+
+def ssim_decimate(ref: np.ndarray, dist: np.ndarray, bitdepth: int,
+                  scale: int = 0, L=None, threads: int = 1):
+    """Frame pairs (n, h, w) of uint8 (bitdepth 8) or uint16 samples ->
+    the decimated fp32 planes (n, sh, sw) of ref and dist.  scale 0 takes
+    the auto scale.  ``threads`` > 1 splits the frames over host threads."""
+    L = L or lib()
+    n, h, w = ref.shape
+    if scale == 0:
+        scale = ssim_auto_scale(w, h, L)
+    sw, sh = ssim_out_size(w, h, scale, L)
+    dt = np.uint8 if bitdepth == 8 else np.uint16
+    ref = np.ascontiguousarray(ref, dt)
+    dist = np.ascontiguousarray(dist, dt)
+    ro = np.zeros((n, sh, sw), np.float32)
+    do = np.zeros((n, sh, sw), np.float32)
+
+    def run(f0, f1):
+        work = np.zeros(w * h, np.float32)
+        rc = L.fso_decimate(ref[f0:f1].ctypes.data, dist[f0:f1].ctypes.data,
+                            w, h, bitdepth, scale, f1 - f0,
+                            _fptr(ro[f0:f1]), _fptr(do[f0:f1]), _fptr(work))
+        if rc:
+            raise ValueError("oracle rejected the frames (rc=%d)" % rc)
+
+    if threads <= 1 or n <= 1:
+        run(0, n)
+    else:
+        step = (n + threads - 1) // threads
+        with ThreadPoolExecutor(max_workers=threads) as ex:
+            list(ex.map(lambda a: run(a, min(n, a + step)),
+                        range(0, n, step)))
+    return ro, do

@@ -74,3 +74,50 @@ def test_planted_mistake_is_caught(mid, old, new, catchers):
         except AssertionError:
             caught.append(pin.__name__)
     assert caught, "no pin noticed the planted mistake %s" % mid
+
+
+import ssim_pins  # noqa: E402
+
+# (id, text in fssim_oracle.c, replacement, pins expected to notice)
+SSIM_MUTATIONS = [
+    ("odd_kernel_offsets", "const int hi = k / 2 - ((k % 2 == 0) ? 1 : 0);",
+     "const int hi = k / 2;", [ssim_pins.pin_exact_window_sum,
+                               ssim_pins.pin_constant_plane]),
+    ("mirror_without_edge_repeat", "return r >= n ? p - 1 - r : r;",
+     "return r >= n ? (p - 2 - r < 0 ? 0 : p - 2 - r) : r;",
+     [ssim_pins.pin_mirror_reflection]),
+    ("float_window_sum", "    double sum = 0.0;\n    for (int dy",
+     "    float sum = 0.0f;\n    for (int dy", [ssim_pins.pin_exact_window_sum]),
+    ("product_not_rounded", "const float prod = img[(size_t)yy * w + xx] * tap;",
+     "const double prod = (double)img[(size_t)yy * w + xx] * tap;",
+     [ssim_pins.pin_exact_window_sum, ssim_pins.pin_constant_plane]),
+    ("size_without_odd_column", "*sw = w / scale + (w & 1);",
+     "*sw = w / scale;", [ssim_pins.pin_out_sizes]),
+    ("tap_one_over_k", "return 1.0f / (float)(scale * scale);",
+     "return 1.0f / (float)scale;", [ssim_pins.pin_tap]),
+    ("auto_scale_truncated", "(int)round((double)m / 256.0);",
+     "m / 256;", [ssim_pins.pin_auto_scale_rounding]),
+    ("centre_off_by_one", "filter_pixel(img, w, h, x * scale, y * scale,",
+     "filter_pixel(img, w, h, x * scale + 1, y * scale,",
+     [ssim_pins.pin_power_of_two_closed_form,
+      ssim_pins.pin_exact_window_sum]),
+    ("sixteen_bit_divisor", "const float div = (float)(1 << (bitdepth - 8));",
+     "const float div = (float)(1 << (bitdepth - 9));",
+     [ssim_pins.pin_scale_one_is_sample_conversion]),
+]
+
+
+@pytest.mark.parametrize("mid,old,new,catchers", SSIM_MUTATIONS,
+                         ids=[m[0] for m in SSIM_MUTATIONS])
+def test_planted_ssim_mistake_is_caught(mid, old, new, catchers):
+    src = oracle.ssim_source()
+    assert src.count(old) == 1, "mutation anchor not found once: %s" % mid
+    L = oracle.build_variant(oracle.source_text(), "ssim_" + mid,
+                             src.replace(old, new))
+    caught = []
+    for pin in catchers:
+        try:
+            pin(L)
+        except AssertionError:
+            caught.append(pin.__name__)
+    assert caught, "no pin noticed the planted mistake %s" % mid
