@@ -1,6 +1,6 @@
 """libfvif.so on the host, without a GPU: it builds for sm_103a, loads,
-exports every entry point include/fvif.h declares, and rejects invalid
-arguments before any CUDA call."""
+exports every entry point the headers under include/ declare, and rejects
+invalid arguments before any CUDA call."""
 import ctypes
 import os
 import re
@@ -12,13 +12,18 @@ import vmaf_float_vif_gb300 as fv
 from vmaf_float_vif_gb300 import _lib
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "fvif.h")
+HEADERS = [os.path.join(ROOT, "include", n)
+           for n in sorted(os.listdir(os.path.join(ROOT, "include")))
+           if n.endswith(".h")]
 
 
 def declared_functions():
-    text = open(HEADER).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(fvif_[a-z_]+)\s*\(", text)))
+    names = set()
+    for path in HEADERS:
+        text = open(path).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names |= set(re.findall(r"\b((?:fvif|fssim)_[a-z_]+)\s*\(", text))
+    return sorted(names)
 
 
 @pytest.fixture(scope="module")
@@ -117,3 +122,53 @@ def test_frame_count_with_stride():
     assert _lib._frames(a, 8, 8, 96) == 3
     with pytest.raises(ValueError):
         _lib._frames(a, 8, 8, 100)
+
+
+def test_both_headers_are_checked():
+    names = [os.path.basename(p) for p in HEADERS]
+    assert "fvif.h" in names and "fssim.h" in names
+    assert "fssim_decimate" in declared_functions()
+
+
+def test_ssim_auto_scale_and_sizes_on_host(L):
+    assert fv.fssim_auto_scale(1920, 1080) == 4
+    assert fv.fssim_auto_scale(3840, 2160) == 8
+    assert fv.fssim_auto_scale(0, 100) == fv.FVIF_EINVAL
+    assert fv.fssim_decimated_size(1920, 1080, 0) == (480, 270)
+    assert fv.fssim_decimated_size(75, 40, 3) == (26, 13)
+    assert fv.fssim_decimated_size(71, 71, 1) == (71, 71)
+    with pytest.raises(fv.FvifError):
+        fv.fssim_decimated_size(64, 64, 129)
+    with pytest.raises(fv.FvifError):
+        fv.fssim_decimated_size(64, 64, -1)
+
+
+@pytest.mark.parametrize("args", [
+    (0, 64, 8, 2), (64, 16385, 8, 2), (64, 64, 7, 2), (64, 64, 17, 2),
+    (64, 64, 8, -1), (64, 64, 8, 129),
+])
+def test_ssim_decimate_rejects_invalid_arguments(L, args):
+    w, h, bd, scale = args
+    buf = ctypes.c_void_p(16)   # never dereferenced: rejected first
+    assert L.fssim_decimate(w, h, bd, scale, buf, buf, 1, buf, buf,
+                            None) == fv.FVIF_EINVAL
+
+
+def test_ssim_decimate_rejects_null_and_misaligned_buffers(L):
+    p = ctypes.c_void_p(4096)
+    null = ctypes.c_void_p(0)
+    assert L.fssim_decimate(64, 64, 8, 2, null, p, 1, p, p, None) == \
+        fv.FVIF_EINVAL
+    assert L.fssim_decimate(64, 64, 8, 2, p, p, 1, p, null, None) == \
+        fv.FVIF_EINVAL
+    assert L.fssim_decimate(64, 64, 8, 2, p, p, 1, ctypes.c_void_p(4098), p,
+                            None) == fv.FVIF_EINVAL
+    assert L.fssim_decimate(64, 64, 10, 2, ctypes.c_void_p(4097), p, 1, p,
+                            p, None) == fv.FVIF_EINVAL
+    assert L.fssim_decimate(64, 64, 8, 2, p, p, -1, p, p, None) == \
+        fv.FVIF_EINVAL
+    # nothing to do: accepted without touching the pointers
+    assert L.fssim_decimate(64, 64, 8, 2, null, null, 0, null, null,
+                            None) == fv.FVIF_OK
+    assert L.fssim_decimate(16, 16, 8, 128, p, p, 1, p, p, None) == \
+        fv.FVIF_OK

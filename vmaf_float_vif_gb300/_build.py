@@ -18,8 +18,10 @@ OUT_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(OUT_DIR, "libfvif.so")
 
 SOURCES = ["fvif_api.cu", "fvif_stats_u8.cu", "fvif_stats_u16.cu",
-           "fvif_stats_f2.cu", "fvif_decimate.cu", "fvif_noalloc.cu"]
-HEADERS = ["fvif_internal.h", "fvif_kernels.cuh", "fvif_dispatch.cuh"]
+           "fvif_stats_f2.cu", "fvif_decimate.cu", "fvif_noalloc.cu",
+           "fssim_api.cu", "fssim_u8.cu", "fssim_u16.cu"]
+HEADERS = ["fvif_internal.h", "fvif_kernels.cuh", "fvif_dispatch.cuh",
+           "fssim_kernels.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "--fmad=false", "-std=c++17",
@@ -37,6 +39,7 @@ def _nvcc() -> str:
 def _inputs():
     paths = [os.path.join(CSRC, s) for s in SOURCES + HEADERS]
     paths.append(os.path.join(INCLUDE, "fvif.h"))
+    paths.append(os.path.join(INCLUDE, "fssim.h"))
     paths.append(os.path.abspath(__file__))
     return paths
 

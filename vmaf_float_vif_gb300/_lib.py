@@ -30,6 +30,8 @@ EXPORTS = (
     "fvif_profile_enable", "fvif_profile_read", "fvif_score_noalloc",
     "fvif_debug_terms", "fvif_default_options", "fvif_create_ex",
     "fvif_score_debug",
+    # include/fssim.h
+    "fssim_auto_scale", "fssim_decimated_size", "fssim_decimate",
 )
 
 
@@ -106,6 +108,13 @@ def _declare(L: ctypes.CDLL) -> ctypes.CDLL:
     L.fvif_debug_terms.restype = i
     L.fvif_score_noalloc.argtypes = [i, i, i, f, d, vp, vp, i, vp, vp]
     L.fvif_score_noalloc.restype = i
+    ip = ctypes.POINTER(ctypes.c_int)
+    L.fssim_auto_scale.argtypes = [i, i]
+    L.fssim_auto_scale.restype = i
+    L.fssim_decimated_size.argtypes = [i, i, i, ip, ip]
+    L.fssim_decimated_size.restype = i
+    L.fssim_decimate.argtypes = [i, i, i, i, vp, vp, i, vp, vp, vp]
+    L.fssim_decimate.restype = i
     return L
 
 
@@ -402,6 +411,61 @@ def fvif_debug_terms(ctx: int, mu1, mu2, xx, yy, xy, count_fallbacks=True):
     if st:
         raise FvifError(st, "fvif_debug_terms")
     return num, den, fb
+
+
+# ---------------------------------------------------------------------------
+# float_ssim auto-scale decimation (include/fssim.h)
+
+
+def fssim_auto_scale(w: int, h: int) -> int:
+    """The auto scale, or FVIF_EINVAL (negative) for a bad size."""
+    return int(lib().fssim_auto_scale(int(w), int(h)))
+
+
+def fssim_decimated_size(w: int, h: int, scale: int = 0) -> Tuple[int, int]:
+    sw, sh = ctypes.c_int(), ctypes.c_int()
+    st = lib().fssim_decimated_size(int(w), int(h), int(scale),
+                                    ctypes.byref(sw), ctypes.byref(sh))
+    if st:
+        raise FvifError(st, "fssim_decimated_size")
+    return sw.value, sh.value
+
+
+def fssim_decimate(ref, dist, w: int, h: int, bitdepth: int, scale: int = 0,
+                   ref_out=None, dist_out=None, stream=None):
+    """Decimate the frame pairs in the device tensors ref and dist (n frames
+    of w*h samples) into fp32 device tensors of shape (n, sh, sw), allocated
+    here when not given.  Enqueued on ``stream`` (default: torch's current
+    stream); returns (ref_out, dist_out) without waiting."""
+    import torch
+    n = _frames(ref, w, h)
+    if _frames(dist, w, h) != n:
+        raise ValueError("ref and dist hold different frame counts")
+    sw, sh = fssim_decimated_size(w, h, scale)
+    for name, t in (("ref_out", ref_out), ("dist_out", dist_out)):
+        if t is not None and (not isinstance(t, torch.Tensor) or not t.is_cuda
+                              or t.dtype != torch.float32
+                              or not t.is_contiguous()
+                              or t.numel() != n * sw * sh):
+            raise ValueError("%s must be a contiguous float32 CUDA tensor "
+                             "of %d values" % (name, n * sw * sh))
+    dev = ref.device
+    if ref_out is None:
+        ref_out = torch.empty((n, sh, sw), dtype=torch.float32, device=dev)
+    if dist_out is None:
+        dist_out = torch.empty((n, sh, sw), dtype=torch.float32, device=dev)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev).cuda_stream
+    elif hasattr(stream, "cuda_stream"):
+        stream = stream.cuda_stream
+    st = lib().fssim_decimate(int(w), int(h), int(bitdepth), int(scale),
+                              _dev_ptr(ref, bitdepth, "ref"),
+                              _dev_ptr(dist, bitdepth, "dist"), n,
+                              ref_out.data_ptr(), dist_out.data_ptr(),
+                              stream)
+    if st:
+        raise FvifError(st, "fssim_decimate")
+    return ref_out, dist_out
 
 
 class Context:

@@ -1,0 +1,609 @@
+/*
+ * fssim_kernels.cuh -- kernels of float_ssim's auto-scale decimation.
+ *
+ * Source: "Research-2130: float_ssim decimation on the SYCL device" (Question:
+ * the auto scale; Sources: the kernel, window offsets, boundary, sample
+ * conversion and decimated size; Findings, "The CPU sum is exact").
+ *
+ * Each output is one fp32 rounding of the exact sum, over a k x k window
+ * (k = scale, period-2n mirror at the edges), of the fp32 products
+ * fl(x * t), x the converted sample and t = fl(1 / k^2).  With x = s * 2^-q
+ * (s the integer sample, q = bitdepth - 8) and t = T * 2^-E (T a 24-bit
+ * integer):
+ *
+ *   fl(x * t) = 2^-q * (s * t - e(s)),   e(s) = s * t - fl(s * t),
+ *
+ * where e(s) is exactly the FMA fma(s, t, -fl(s * t)) and an integer
+ * multiple of 2^-E with |e| <= 2^15 * 2^-E.  So the window sum is
+ *
+ *   2^-(q + E) * (T * sum(s) - sum(e * 2^E))
+ *
+ * with both sums integers: sum(s) <= k^2 * 65535 < 2^31 and
+ * |sum(e * 2^E)| <= k^2 * 2^15 <= 2^29 for k <= 128.  The int64 total is
+ * rounded once to fp32 (__ll2float_rn), and the power-of-two factor is
+ * applied exactly.  For power-of-two k the tap is exact: e = 0 and the output
+ * is fl(sum(s)) * t * 2^-q.
+ *
+ * Work split: a block takes R output rows by X output columns of one plane of
+ * one frame.  Phase 1: each thread sums V adjacent input columns (one 16-byte
+ * load per row on the vector path) over the k window rows of its output
+ * rows, into sum(s) as integers and sum(e) as fp32.  The fp32 sum is exact:
+ * each partial sum is a multiple of 2^-E below k * 2^15 * 2^-E < 2^24 * 2^-E.
+ * The loads of a batch of rows are all issued before any is added.  The
+ * column sums go to shared memory as integers.  Phase 2: each thread adds the
+ * k columns of one output window, mirrored at the edges, and rounds once.
+ * Every input byte is read from DRAM once (edge windows re-read mirrored
+ * columns from shared memory), so the kernel is bound by HBM bandwidth.
+ *
+ * The scales 2..8 (the auto scales of frames up to 8.5K wide) are compiled
+ * with k fixed, so the row and column loops unroll; other scales run the same
+ * kernel with k read at run time.
+ */
+#ifndef FSSIM_KERNELS_CUH
+#define FSSIM_KERNELS_CUH
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+namespace fssim {
+
+constexpr int kThreads = 256;
+constexpr int kMaxTileCols = 4096;          // window columns per tile row
+constexpr int kMaxRows = 16;                // output rows per block
+constexpr size_t kMaxSmem = 64 * 1024;      // shared bytes per block
+constexpr int kMaxFramesPerLaunch = 32767;  // grid.z = 2 * frames
+constexpr int kBatch = 8;                   // rows loaded before any is added
+constexpr int kMaxFixedScale = 8;           // scales compiled with k fixed
+
+struct DecimateParams {
+    const void *src[2];       // ref, dist
+    float *dst[2];
+    size_t in_frame_elems;
+    size_t out_frame_elems;
+    int w, h, k, sw, sh;
+    int X, R;                 // outputs per tile row, output rows per block
+    int pitch;                // shared row pitch in ints (skewed)
+    float tap;                // fl(1 / k^2)
+    float err_scale;          // 2^E: e * 2^E is an integer
+    long long T;              // tap = T * 2^-E
+    float out_scale;          // 2^-(q + E), or tap * 2^-q for exact taps
+    int packed16;             // 16-bit samples: column sums fit 16 bits
+};
+
+/* Period-2n symmetric mirror: -1 -> 0, n -> n - 1, repeating with period 2n. */
+__device__ __forceinline__ int mirror2n(int j, int n)
+{
+    if (j >= 0 && j < n)
+        return j;
+    const int p = 2 * n;
+    int r = j % p;
+    if (r < 0)
+        r += p;
+    return r >= n ? p - 1 - r : r;
+}
+
+/* Shared-memory column index with one padding word per 32: the phase-1
+ * stores (V consecutive columns per thread) and the phase-2 reads (stride k)
+ * then fall on distinct banks for V = 8, 16 and k = 2 .. 32 powers of two.
+ * A group of V | 32 columns starting at a multiple of V shares one offset. */
+__device__ __forceinline__ int skew(int c) { return c + (c >> 5); }
+
+/* Column accumulators of one thread: V adjacent input columns.
+ *  - sample sums: for 8-bit samples two 16-bit lanes per register
+ *    (k * 255 < 2^16), columns (0, 2) and (1, 3) of each 4-byte word; for
+ *    16-bit samples one register per column, or two 16-bit lanes per word when
+ *    k * (2^bitdepth - 1) < 2^16 (packed16);
+ *  - product errors (inexact taps only): one fp32 per column. */
+template <typename T, bool kExactTap>
+struct ColAcc {
+    static constexpr int V = 16 / sizeof(T);
+    unsigned s[8];
+    float e[V];
+
+    __device__ __forceinline__ void reset()
+    {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            s[i] = 0u;
+#pragma unroll
+        for (int v = 0; v < V; ++v)
+            e[v] = 0.0f;
+    }
+
+    /* fp32 value of sample v of the 16-byte vector (exact: 2^23 + s - 2^23) */
+    __device__ __forceinline__ static float sample_f(const uint4 &q, int v)
+    {
+        const unsigned w = v < V / 4 ? q.x : v < V / 2 ? q.y
+                                   : v < 3 * V / 4 ? q.z : q.w;
+        unsigned bits;
+        if (sizeof(T) == 1)
+            bits = __byte_perm(w, 0x4B000000u, 0x7540u | (unsigned)(v & 3));
+        else
+            bits = __byte_perm(w, 0x4B000000u, (v & 1) ? 0x7432u : 0x7410u);
+        return __fsub_rn(__uint_as_float(bits), 8388608.0f);
+    }
+
+    __device__ __forceinline__ void add(const uint4 &q, bool packed16,
+                                        float tap)
+    {
+        const unsigned w[4] = {q.x, q.y, q.z, q.w};
+        if (sizeof(T) == 1) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                s[2 * j] += __byte_perm(w[j], 0u, 0x4240u);
+                s[2 * j + 1] += __byte_perm(w[j], 0u, 0x4341u);
+            }
+        } else if (packed16) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                s[j] += w[j];
+        } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                s[2 * j] += w[j] & 0xffffu;
+                s[2 * j + 1] += w[j] >> 16;
+            }
+        }
+        if (!kExactTap) {
+#pragma unroll
+            for (int v = 0; v < V; ++v) {
+                const float xf = sample_f(q, v);
+                const float prod = __fmul_rn(xf, tap);
+                e[v] = __fadd_rn(e[v], __fmaf_rn(xf, tap, -prod));
+            }
+        }
+    }
+
+    /* sample sum of column v */
+    __device__ __forceinline__ int col(int v, bool packed16) const
+    {
+        if (sizeof(T) == 1) {
+            const unsigned r = s[2 * (v >> 2) + (v & 1)];
+            return (int)((v & 2) ? r >> 16 : r & 0xffffu);
+        }
+        if (packed16) {
+            const unsigned r = s[v >> 1];
+            return (int)((v & 1) ? r >> 16 : r & 0xffffu);
+        }
+        return (int)s[v];
+    }
+
+    /* write the V column sums of group g to one output row's arrays */
+    __device__ __forceinline__ void store(int *rowS, int *rowE, int g,
+                                          bool packed16, float err_scale) const
+    {
+        const int base = skew(g * V);
+#pragma unroll
+        for (int v = 0; v < V; ++v) {
+            rowS[base + v] = col(v, packed16);
+            if (!kExactTap)
+                rowE[base + v] =
+                    __float2int_rn(__fmul_rn(e[v], err_scale));
+        }
+    }
+};
+
+/* V samples starting at column c0 of row rp, packed as a 16-byte vector
+ * (little-endian, as a vector load would give); columns >= w read as 0. */
+template <typename T, bool kVec>
+__device__ __forceinline__ uint4 load_group(const T *rp, int c0, int w)
+{
+    if (kVec)
+        return __ldg(reinterpret_cast<const uint4 *>(rp + c0));
+    constexpr int V = 16 / sizeof(T);
+    unsigned wd[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+        const unsigned x = (c0 + v < w) ? (unsigned)__ldg(rp + c0 + v) : 0u;
+        wd[v * sizeof(T) / 4] |= x << (8 * ((v * sizeof(T)) & 3));
+    }
+    return make_uint4(wd[0], wd[1], wd[2], wd[3]);
+}
+
+/* K > 0: k fixed at compile time (2..8); K == 0: k = p.k at run time. */
+template <typename T, int K, bool kExactTap, bool kVec>
+__global__ void __launch_bounds__(kThreads)
+ssim_decimate_kernel(const DecimateParams p)
+{
+    constexpr int V = 16 / sizeof(T);
+    /* output rows whose K input rows fill one load batch (fixed k) */
+    constexpr int kRowsPerBatch = K > 0 ? (kBatch / K > 0 ? kBatch / K : 1) : 1;
+    extern __shared__ int shm[];
+    int *sS = shm;                        // R rows of column sample sums
+    int *sE = shm + p.R * p.pitch;        // R rows of column error sums
+
+    const int plane = blockIdx.z & 1;
+    const size_t f = blockIdx.z >> 1;
+    /* select, not index: a run-time index into the parameter arrays would
+     * copy them to local memory */
+    const T *src = static_cast<const T *>(plane ? p.src[1] : p.src[0]) +
+                   f * p.in_frame_elems;
+    float *dst = (plane ? p.dst[1] : p.dst[0]) + f * p.out_frame_elems;
+    const int k = K > 0 ? K : p.k;
+    const int w = p.w, h = p.h, half = k >> 1;
+    const int x0 = blockIdx.x * p.X;
+    const int xn = min(p.X, p.sw - x0);
+    const int y0 = blockIdx.y * p.R;
+    const int rn = min(p.R, p.sh - y0);
+
+    /* Input columns the tile's windows touch, after mirroring. */
+    const int J0 = k * x0 - half;
+    const int J1 = J0 + xn * k - 1;
+    const bool interior = J0 >= 0 && J1 < w;
+    int C0 = 0, C1 = w - 1;
+    if (J0 >= -w && J1 < 2 * w) {
+        C0 = max(J0, 0);
+        C1 = min(J1, w - 1);
+        if (J0 < 0)
+            C1 = max(C1, min(w - 1, -1 - J0));
+        if (J1 >= w)
+            C0 = min(C0, max(0, 2 * w - 1 - J1));
+    }
+    const int Ca = kVec ? (C0 & ~(V - 1)) : C0;
+    const int G = (C1 + 1 - Ca + V - 1) / V;
+
+    /* Phase 1: thread (g, sub) sums column group g over the k input rows of
+     * output rows sub, sub + m, sub + 2m, ... */
+    const int m = kThreads / G > 0 ? kThreads / G : 1;
+    for (int t = threadIdx.x; t < G * m; t += kThreads) {
+        const int g = t % G;
+        const int sub = t / G;
+        const int nr = sub < rn ? (rn - 1 - sub) / m + 1 : 0;
+        const int c0 = Ca + g * V;
+        const T *col0 = src + c0;
+        ColAcc<T, kExactTap> acc;
+        acc.reset();
+        if (K > 0) {
+            /* whole output rows per batch: kRowsPerBatch * K loads */
+            for (int rb = 0; rb < nr; rb += kRowsPerBatch) {
+                uint4 q[kRowsPerBatch][K > 0 ? K : 1];
+#pragma unroll
+                for (int b = 0; b < kRowsPerBatch; ++b) {
+                    if (rb + b < nr) {
+                        const int yb = k * (y0 + sub + (rb + b) * m) - half;
+#pragma unroll
+                        for (int i = 0; i < (K > 0 ? K : 1); ++i)
+                            q[b][i] = load_group<T, kVec>(
+                                col0 + (size_t)mirror2n(yb + i, h) * w,
+                                0, w - c0);
+                    }
+                }
+#pragma unroll
+                for (int b = 0; b < kRowsPerBatch; ++b) {
+                    if (rb + b < nr) {
+#pragma unroll
+                        for (int i = 0; i < (K > 0 ? K : 1); ++i)
+                            acc.add(q[b][i], p.packed16, p.tap);
+                        const int r = sub + (rb + b) * m;
+                        acc.store(sS + r * p.pitch, sE + r * p.pitch, g,
+                                  p.packed16, p.err_scale);
+                        acc.reset();
+                    }
+                }
+            }
+        } else {
+            /* run-time k: batches of kBatch input rows; input row u of this
+             * thread is row i of its output row ri */
+            const int total = nr * k;
+            int ri0 = 0, i0 = 0;
+            for (int u0 = 0; u0 < total; u0 += kBatch) {
+                uint4 q[kBatch];
+                int ri = ri0, i = i0;
+#pragma unroll
+                for (int j = 0; j < kBatch; ++j) {
+                    if (u0 + j < total) {
+                        const int y = k * (y0 + sub + ri * m) - half + i;
+                        q[j] = load_group<T, kVec>(
+                            col0 + (size_t)mirror2n(y, h) * w, 0, w - c0);
+                    }
+                    if (++i == k) {
+                        i = 0;
+                        ++ri;
+                    }
+                }
+                ri = ri0;
+                i = i0;
+#pragma unroll
+                for (int j = 0; j < kBatch; ++j) {
+                    const bool row_end = i == k - 1;
+                    const int r = sub + ri * m;
+                    if (++i == k) {
+                        i = 0;
+                        ++ri;
+                    }
+                    if (u0 + j < total) {
+                        acc.add(q[j], p.packed16, p.tap);
+                        if (row_end) {
+                            acc.store(sS + r * p.pitch, sE + r * p.pitch, g,
+                                      p.packed16, p.err_scale);
+                            acc.reset();
+                        }
+                    }
+                }
+                ri0 = ri;
+                i0 = i;
+            }
+        }
+    }
+    __syncthreads();
+
+    /* Phase 2: each output adds its window's k columns and rounds once. */
+    for (int r = 0; r < rn; ++r) {
+        const int *rowS = sS + r * p.pitch;
+        const int *rowE = sE + r * p.pitch;
+        float *orow = dst + (size_t)(y0 + r) * p.sw;
+        for (int xo = threadIdx.x; xo < xn; xo += kThreads) {
+            const int x = x0 + xo;
+            const int jb = k * x - half;
+            int S = 0, E = 0;
+            if (interior || (jb >= 0 && jb + k <= w)) {
+                const int cb = jb - Ca;
+                /* fixed k: the unrolled loop; run-time k: the second */
+#pragma unroll
+                for (int i = 0; i < K; ++i) {
+                    const int c = skew(cb + i);
+                    S += rowS[c];
+                    if (!kExactTap)
+                        E += rowE[c];
+                }
+                for (int i = K; i < k; ++i) {
+                    const int c = skew(cb + i);
+                    S += rowS[c];
+                    if (!kExactTap)
+                        E += rowE[c];
+                }
+            } else {
+                for (int i = 0; i < k; ++i) {
+                    const int c = skew(mirror2n(jb + i, w) - Ca);
+                    S += rowS[c];
+                    if (!kExactTap)
+                        E += rowE[c];
+                }
+            }
+            float out;
+            if (kExactTap)
+                out = __fmul_rn(__int2float_rn(S), p.out_scale);
+            else
+                out = __fmul_rn(
+                    __ll2float_rn(p.T * (long long)S - (long long)E),
+                    p.out_scale);
+            orow[x] = out;
+        }
+    }
+}
+
+/* 8-bit samples, k = 4 or 8, rows a multiple of 16 bytes: every window
+ * either lies inside one 16-column group or straddles a group boundary with
+ * k/2 columns on each side.  Each thread loads its group's 16 bytes from
+ * each of the k input rows of an output row and forms the window partial
+ * sums with dp4a (byte masks select the window's columns): the left half of
+ * the straddling window, the inner windows, the right half of the next
+ * straddling window.  The straddling window at the group's start adds the
+ * left neighbour's right half, taken by shuffle from lane - 1; lane 0 (or the
+ * first group of a block column) reloads that neighbour's last word, and
+ * group 0 mirrors its own left half.  The last window of a row is always an
+ * inner one (w even and a multiple of 16), so the right edge needs no
+ * mirror.  Outputs are written as one 8-byte (k = 8) or 16-byte (k = 4)
+ * store per thread.  No shared memory, no block barrier. */
+template <int K>
+__global__ void __launch_bounds__(kThreads)
+ssim_decimate_u8_partials_kernel(const DecimateParams p)
+{
+    static_assert(K == 4 || K == 8, "window partials for k = 4 and 8");
+    constexpr int kOut = 16 / K;          // windows starting in a group
+    constexpr int kHalf = K / 2;
+    const int plane = blockIdx.z & 1;
+    const size_t f = blockIdx.z >> 1;
+    const unsigned char *src =
+        static_cast<const unsigned char *>(plane ? p.src[1] : p.src[0]) +
+        f * p.in_frame_elems;
+    float *dst = (plane ? p.dst[1] : p.dst[0]) + f * p.out_frame_elems;
+    const int w = p.w, h = p.h;
+    const int G = w >> 4;                 // groups per row
+    const int Gb = p.X;                   // groups per block column
+    const int m = kThreads / Gb;          // output rows walked side by side
+    const int t = threadIdx.x;
+    const int gi = t % Gb;
+    const int sub = t / Gb;
+    const int g = blockIdx.x * Gb + gi;
+    const bool col_ok = sub < m && g < G;
+    const int lane = t & 31;
+    /* thread t - 1 holds group g - 1 of the same output row */
+    const bool nb_in_warp = lane > 0 && gi > 0;
+    const int y0 = blockIdx.y * p.R;
+    const int rn = min(p.R, p.sh - y0);
+    const int iters = (p.R + m - 1) / m;
+    const unsigned char *colp = src + 16 * (size_t)g;
+
+    for (int it = 0; it < iters; ++it) {
+        const int r = sub + it * m;
+        const bool act = col_ok && r < rn;
+        const int yb = K * (y0 + r) - kHalf;
+        uint4 q[K];
+        unsigned prev[K];
+        if (act) {
+#pragma unroll
+            for (int i = 0; i < K; ++i) {
+                const unsigned char *rp =
+                    colp + (size_t)mirror2n(yb + i, h) * w;
+                q[i] = __ldg(reinterpret_cast<const uint4 *>(rp));
+                if (!nb_in_warp && g > 0)
+                    prev[i] = __ldg(reinterpret_cast<const unsigned *>(rp) - 1);
+            }
+        }
+        unsigned left = 0u, right = 0u, inner[kOut - 1];
+#pragma unroll
+        for (int j = 0; j < kOut - 1; ++j)
+            inner[j] = 0u;
+        if (act) {
+#pragma unroll
+            for (int i = 0; i < K; ++i) {
+                if constexpr (K == 8) {
+                    left = __dp4a(q[i].x, 0x01010101u, left);
+                    inner[0] = __dp4a(q[i].y, 0x01010101u, inner[0]);
+                    inner[0] = __dp4a(q[i].z, 0x01010101u, inner[0]);
+                    right = __dp4a(q[i].w, 0x01010101u, right);
+                } else {
+                    left = __dp4a(q[i].x, 0x00000101u, left);
+                    inner[0] = __dp4a(q[i].x, 0x01010000u, inner[0]);
+                    inner[0] = __dp4a(q[i].y, 0x00000101u, inner[0]);
+                    inner[1] = __dp4a(q[i].y, 0x01010000u, inner[1]);
+                    inner[1] = __dp4a(q[i].z, 0x00000101u, inner[1]);
+                    inner[2] = __dp4a(q[i].z, 0x01010000u, inner[2]);
+                    inner[2] = __dp4a(q[i].w, 0x00000101u, inner[2]);
+                    right = __dp4a(q[i].w, 0x01010000u, right);
+                }
+            }
+        }
+        const unsigned from_left = __shfl_up_sync(0xffffffffu, right, 1);
+        if (act) {
+            unsigned prev_right;
+            if (nb_in_warp) {
+                prev_right = from_left;
+            } else if (g == 0) {
+                prev_right = left;       // mirrored: [-k/2, 0) -> [0, k/2)
+            } else {
+                prev_right = 0u;
+#pragma unroll
+                for (int i = 0; i < K; ++i)
+                    prev_right = __dp4a(prev[i], K == 8 ? 0x01010101u
+                                                        : 0x01010000u,
+                                        prev_right);
+            }
+            float o[kOut];
+            o[0] = __fmul_rn(__uint2float_rn(prev_right + left), p.out_scale);
+#pragma unroll
+            for (int j = 1; j < kOut; ++j)
+                o[j] = __fmul_rn(__uint2float_rn(inner[j - 1]), p.out_scale);
+            float *orow = dst + (size_t)(y0 + r) * p.sw + kOut * g;
+            if constexpr (K == 8)
+                *reinterpret_cast<float2 *>(orow) = make_float2(o[0], o[1]);
+            else
+                *reinterpret_cast<float4 *>(orow) =
+                    make_float4(o[0], o[1], o[2], o[3]);
+        }
+    }
+}
+
+/* Scale 1: the converted samples. */
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+ssim_convert_kernel(const T *ref, const T *dist, float *ref_out,
+                    float *dist_out, size_t n, float inv)
+{
+    const size_t stride = (size_t)gridDim.x * blockDim.x;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+         i += stride) {
+        ref_out[i] = __fmul_rn((float)ref[i], inv);
+        dist_out[i] = __fmul_rn((float)dist[i], inv);
+    }
+}
+
+template <typename T, int K, bool kExactTap, bool kVec>
+cudaError_t launch(const DecimateParams &p, int n_frames, size_t smem,
+                   cudaStream_t stream)
+{
+    auto kern = ssim_decimate_kernel<T, K, kExactTap, kVec>;
+    cudaError_t e = cudaFuncSetAttribute(
+        kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess)
+        return e;
+    DecimateParams q = p;
+    const size_t in_bytes = p.in_frame_elems * sizeof(T);
+    for (int f0 = 0; f0 < n_frames; f0 += kMaxFramesPerLaunch) {
+        const int nf = n_frames - f0 < kMaxFramesPerLaunch
+                           ? n_frames - f0 : kMaxFramesPerLaunch;
+        for (int s = 0; s < 2; ++s) {
+            q.src[s] = static_cast<const unsigned char *>(p.src[s]) +
+                       in_bytes * (size_t)f0;
+            q.dst[s] = p.dst[s] + p.out_frame_elems * (size_t)f0;
+        }
+        const dim3 grid((p.sw + p.X - 1) / p.X, (p.sh + p.R - 1) / p.R,
+                        2 * nf);
+        kern<<<grid, kThreads, smem, stream>>>(q);
+        e = cudaGetLastError();
+        if (e != cudaSuccess)
+            return e;
+    }
+    return cudaSuccess;
+}
+
+/* Launch shape of the 8-bit window-partials kernel: p.X groups per block
+ * column, p.R output rows per block. */
+template <int K>
+cudaError_t launch_partials(DecimateParams p, int n_frames,
+                            cudaStream_t stream)
+{
+    const int G = p.w >> 4;
+    p.X = G < kThreads ? G : kThreads;
+    const int m = kThreads / p.X;
+    p.R = 2 * m < p.sh ? 2 * m : p.sh;
+    DecimateParams q = p;
+    const size_t in_bytes = p.in_frame_elems;
+    for (int f0 = 0; f0 < n_frames; f0 += kMaxFramesPerLaunch) {
+        const int nf = n_frames - f0 < kMaxFramesPerLaunch
+                           ? n_frames - f0 : kMaxFramesPerLaunch;
+        for (int s = 0; s < 2; ++s) {
+            q.src[s] = static_cast<const unsigned char *>(p.src[s]) +
+                       in_bytes * (size_t)f0;
+            q.dst[s] = p.dst[s] + p.out_frame_elems * (size_t)f0;
+        }
+        const dim3 grid((G + p.X - 1) / p.X, (p.sh + p.R - 1) / p.R, 2 * nf);
+        ssim_decimate_u8_partials_kernel<K><<<grid, kThreads, 0, stream>>>(q);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess)
+            return e;
+    }
+    return cudaSuccess;
+}
+
+template <typename T, int K>
+cudaError_t launch_fixed(const DecimateParams &p, bool vec, int n_frames,
+                         size_t smem, cudaStream_t stream)
+{
+    constexpr bool kExact = (K & (K - 1)) == 0;
+    return vec ? launch<T, K, kExact, true>(p, n_frames, smem, stream)
+               : launch<T, K, kExact, false>(p, n_frames, smem, stream);
+}
+
+/* All kernels for one sample type (defined in fssim_u8.cu / fssim_u16.cu). */
+template <typename T>
+cudaError_t dispatch(const DecimateParams &p, bool exact, bool vec,
+                     int n_frames, size_t smem, cudaStream_t stream);
+
+template <typename T>
+cudaError_t dispatch_impl(const DecimateParams &p, bool exact, bool vec,
+                          int n_frames, size_t smem, cudaStream_t stream)
+{
+    /* 8-bit, k = 4 or 8, 16-byte rows and 16-byte aligned outputs */
+    if (sizeof(T) == 1 && vec && (p.k == 4 || p.k == 8) && p.w % 16 == 0 &&
+        ((uintptr_t)p.dst[0] | (uintptr_t)p.dst[1]) % 16 == 0)
+        return p.k == 4 ? launch_partials<4>(p, n_frames, stream)
+                        : launch_partials<8>(p, n_frames, stream);
+    switch (p.k) {
+    case 2: return launch_fixed<T, 2>(p, vec, n_frames, smem, stream);
+    case 3: return launch_fixed<T, 3>(p, vec, n_frames, smem, stream);
+    case 4: return launch_fixed<T, 4>(p, vec, n_frames, smem, stream);
+    case 5: return launch_fixed<T, 5>(p, vec, n_frames, smem, stream);
+    case 6: return launch_fixed<T, 6>(p, vec, n_frames, smem, stream);
+    case 7: return launch_fixed<T, 7>(p, vec, n_frames, smem, stream);
+    case 8: return launch_fixed<T, 8>(p, vec, n_frames, smem, stream);
+    default: break;
+    }
+    if (exact)
+        return vec ? launch<T, 0, true, true>(p, n_frames, smem, stream)
+                   : launch<T, 0, true, false>(p, n_frames, smem, stream);
+    return vec ? launch<T, 0, false, true>(p, n_frames, smem, stream)
+               : launch<T, 0, false, false>(p, n_frames, smem, stream);
+}
+
+template <typename T>
+cudaError_t convert(const void *ref, const void *dist, float *ref_out,
+                    float *dist_out, size_t n, float inv,
+                    cudaStream_t stream);
+
+} // namespace fssim
+
+#endif /* FSSIM_KERNELS_CUH */

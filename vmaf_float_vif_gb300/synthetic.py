@@ -190,6 +190,14 @@ def _cases() -> Dict[str, Case]:
 CASES: Dict[str, Case] = _cases()
 
 
+def video_case(w: int, h: int, bitdepth: int, frames: int = 3,
+               seed: int = 0) -> Case:
+    """1/f texture reference with a blurred, noisy, block-quantised
+    distorted copy (the 4K workload's recipe) at any size and bit depth."""
+    return Case("video_%dx%d_%db" % (w, h, bitdepth), w, h, bitdepth, frames,
+                _video(w, h, seed, bitdepth))
+
+
 def custom_noise_case(w: int, h: int, bitdepth: int, frames: int = 1,
                       seed: int = 7, smooth: bool = True) -> Case:
     """Noise pair of any size and bit depth (edge sizes, ragged tiles)."""
