@@ -373,6 +373,7 @@ def run_ours(args):
                "ms_per_step": 1e3 * wall / args.e2e_steps,
                "api": "fvif_score_host (page-locked host inputs)",
                "step_ms": [round(t, 2) for t in step_ms],
+               "median_step_ms": float(np.median(step_ms)),
                "h2d_link_gbs": [round(link, 1), round(link_after, 1)],
                "link_floor_ms": 1e3 * (ref.nbytes + dist_np.nbytes) / 1e9 / link,
                "link_note": "plain page-locked 1 GiB host-to-device copy, best "
@@ -474,6 +475,9 @@ def run_ours(args):
     ctx.close()
     if args.also and args.also != args.workload:
         line["also"] = secondary(args.also, args)
+    if not args.no_ssim:
+        line["ssim_decimate"] = ssim_decimate_lines(
+            args, hbm_peak, hbm_src, cpu_baseline=not args.no_cpu_baseline)
     if e2e:
         line["e2e"] = e2e
     if not args.no_cpu_baseline:
@@ -488,6 +492,126 @@ def run_ours(args):
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+# float_ssim auto-scale decimation: name -> (w, h, bitdepth, frames per launch)
+SSIM_WORKLOADS = {
+    "ssim_dec_4k_8b": (3840, 2160, 8, 64),
+    "ssim_dec_720p_8b": (1280, 720, 8, 512),
+}
+SSIM_TRAFFIC_PATH = os.path.join(ROOT, "profiles", "ssim_decimate_traffic.json")
+SSIM_KERNEL_SOURCES = ["fssim_kernels.cuh", "fssim_u8.cu", "fssim_u16.cu",
+                       "fssim_api.cu"]
+
+
+def ssim_kernel_hash():
+    h = hashlib.sha256()
+    for n in SSIM_KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "vmaf_float_vif_gb300", "csrc", n),
+                  "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ssim_traffic(name):
+    try:
+        with open(SSIM_TRAFFIC_PATH) as f:
+            t = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if t.get("kernel_hash") != ssim_kernel_hash():
+        return None
+    return t.get("per_launch_bytes", {}).get(name)
+
+
+def ssim_decimate_lines(args, hbm_peak, hbm_src, cpu_baseline=True):
+    """float_ssim's auto-scale decimation of frame pairs (a second workload
+    of the library): one fssim_decimate launch of F frame pairs per step,
+    device-resident inputs larger than L2, CUDA events on the launching
+    stream; the HBM roofline counts the input samples read once and the
+    fp32 planes written once."""
+    import torch
+    import vmaf_float_vif_gb300 as fv
+    out = {}
+    for name, (w, h, bd, frames) in SSIM_WORKLOADS.items():
+        case = S.video_case(w, h, bd, frames=8, seed=21)
+        ref, dist_np = S.streamed_batch(case, frames, distinct=8)
+
+        def as_dev(a):
+            return torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16
+                                    else a).to("cuda")
+        r, d = as_dev(ref), as_dev(dist_np)
+        scale = fv.fssim_auto_scale(w, h)
+        sw, sh = fv.fssim_decimated_size(w, h, scale)
+        ro = torch.empty((frames, sh, sw), dtype=torch.float32, device="cuda")
+        do = torch.empty_like(ro)
+        stream = torch.cuda.Stream()
+        with torch.cuda.stream(stream):
+            for _ in range(max(3, args.warmup)):
+                fv.fssim_decimate(r, d, w, h, bd, 0, ro, do, stream)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            fv.fssim_decimate(r, d, w, h, bd, 0, ro, do, stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / args.steps
+        B = 1 if bd == 8 else 2
+        per_pair = 2 * w * h * B + 2 * sw * sh * 4
+        achieved = frames * per_pair / (ms / 1e3) / 1e9
+        entry = {
+            "workload": "%dx%d %d-bit, auto scale %d -> %dx%d, %d frame "
+                        "pairs per launch (%.2f GB, larger than L2)" %
+                        (w, h, bd, scale, sw, sh, frames,
+                         frames * 2 * w * h * B / 1e9),
+            "value": frames / (ms / 1e3), "unit": "frame-pairs/s",
+            "ms_per_launch": ms,
+            "roofline": {
+                "bound": "hbm", "achieved": achieved, "peak": hbm_peak,
+                "unit": "GB/s", "frac": achieved / hbm_peak,
+                "peak_note": hbm_src,
+                "traffic": ssim_traffic(name),
+                "per_unit": "%d bytes per frame pair (samples read once, "
+                            "fp32 planes written once)" % per_pair,
+            },
+        }
+        if cpu_baseline:
+            import oracle
+            cores = host_cores()
+            n = min(frames, 2 * cores)
+            t0 = time.perf_counter()
+            oracle.ssim_decimate(ref[:n], dist_np[:n], bd, 0, threads=cores)
+            dt = time.perf_counter() - t0
+            entry["cpu_baseline"] = {
+                "value": n / dt, "unit": "frame-pairs/s", "cores": cores,
+                "kind": "oracle",
+                "sample": "%d frame pairs of the workload over %d host "
+                          "threads, %.1f s wall" % (n, cores, dt)}
+        out[name] = entry
+        del r, d, ro, do
+        torch.cuda.empty_cache()
+    return out
+
+
+def run_ssim_only(args):
+    import torch
+    import vmaf_float_vif_gb300 as fv
+    fv.build()
+    torch.cuda.init()
+    peaks = {}
+    try:
+        with open(PEAKS_PATH) as f:
+            peaks = json.load(f)
+    except (OSError, ValueError):
+        pass
+    hbm_peak = peaks.get("hbm_gbs")
+    hbm_src = "of measured" if hbm_peak else "of fallback"
+    lines = ssim_decimate_lines(args, hbm_peak or FALLBACK_HBM_GBS, hbm_src,
+                                cpu_baseline=not args.no_cpu_baseline)
+    print(json.dumps({"ssim_decimate": lines, "steps": args.steps,
+                      "warmup": max(3, args.warmup)}), flush=True)
 
 
 def secondary(name, args):
@@ -581,9 +705,15 @@ def main():
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="c5_4k_10b")
     ap.add_argument("--frames", type=int, default=None,
                     help="frames per step (default: the workload's)")
-    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-ssim", action="store_true",
+                    help="skip the float_ssim decimation measurement")
+    ap.add_argument("--ssim-only", action="store_true",
+                    help="only the float_ssim decimation measurement (one "
+                         "JSON line; the small case the decimation profiles "
+                         "are captured on)")
     ap.add_argument("--also", choices=sorted(WORKLOADS) + [""],
                     default="c2_1080p_10b",
                     help="second workload timed device-resident (\"\" = none)")
@@ -592,6 +722,8 @@ def main():
         print("note: fewer than 3 warm-up steps", file=sys.stderr)
     if args.impl == "reference":
         run_reference(args)
+    elif args.ssim_only:
+        run_ssim_only(args)
     else:
         run_ours(args)
 

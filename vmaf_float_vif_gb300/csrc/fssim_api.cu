@@ -106,6 +106,7 @@ extern "C" int fssim_decimate(int w, int h, int bitdepth, int scale,
     const bool exact = (k & (k - 1)) == 0;
     p.out_scale = exact ? p.tap * inv_q : std::ldexp(1.0f, -(q + E));
     p.packed16 = B == 2 && (long long)k * ((1 << bitdepth) - 1) < 65536;
+    p.one2 = make_float2(1.0f, 1.0f);
 
     /* Tile: up to kMaxTileCols window columns (whole rows at 4K); shared
      * rows hold the groups of V columns those windows touch. */

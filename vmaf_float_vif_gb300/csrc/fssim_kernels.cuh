@@ -70,6 +70,7 @@ struct DecimateParams {
     long long T;              // tap = T * 2^-E
     float out_scale;          // 2^-(q + E), or tap * 2^-q for exact taps
     int packed16;             // 16-bit samples: column sums fit 16 bits
+    float2 one2;              // (1, 1)
 };
 
 /* Period-2n symmetric mirror: -1 -> 0, n -> n - 1, repeating with period 2n. */
@@ -90,30 +91,77 @@ __device__ __forceinline__ int mirror2n(int j, int n)
  * A group of V | 32 columns starting at a multiple of V shares one offset. */
 __device__ __forceinline__ int skew(int c) { return c + (c >> 5); }
 
+/* Packed two-lane fp32 operations (.f32x2, one issue slot for two lanes).
+ * Each lane rounds once, as the scalar __fmul_rn / __fmaf_rn do.  Sums are
+ * formed as fma(x, one, acc) with one = (1, 1) read from the launch
+ * arguments, so the code generator cannot merge a product into them. */
+__device__ __forceinline__ float2 mul2_rn(float2 a, float2 b)
+{
+    float2 r;
+    asm("{\n\t.reg .b64 pa, pb, pd;\n\t"
+        "mov.b64 pa, {%2, %3};\n\t"
+        "mov.b64 pb, {%4, %5};\n\t"
+        "mul.rn.f32x2 pd, pa, pb;\n\t"
+        "mov.b64 {%0, %1}, pd;\n\t}"
+        : "=f"(r.x), "=f"(r.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return r;
+}
+
+__device__ __forceinline__ float2 fma2_rn(float2 a, float2 b, float2 c)
+{
+    float2 r;
+    asm("{\n\t.reg .b64 pa, pb, pc, pd;\n\t"
+        "mov.b64 pa, {%2, %3};\n\t"
+        "mov.b64 pb, {%4, %5};\n\t"
+        "mov.b64 pc, {%6, %7};\n\t"
+        "fma.rn.f32x2 pd, pa, pb, pc;\n\t"
+        "mov.b64 {%0, %1}, pd;\n\t}"
+        : "=f"(r.x), "=f"(r.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return r;
+}
+
+/* Constants of the inexact-tap arithmetic, passed as launch arguments. */
+struct PairConsts {
+    float2 one;      // (1, 1)
+    float2 m23;      // (-2^23, -2^23)
+    float2 tap;      // (t, t)
+    float2 ntap;     // (-t, -t)
+};
+
 /* Column accumulators of one thread: V adjacent input columns.
- *  - sample sums: for 8-bit samples two 16-bit lanes per register
- *    (k * 255 < 2^16), columns (0, 2) and (1, 3) of each 4-byte word; for
- *    16-bit samples one register per column, or two 16-bit lanes per word when
- *    k * (2^bitdepth - 1) < 2^16 (packed16);
- *  - product errors (inexact taps only): one fp32 per column. */
+ * Exact taps (powers of two): sample sums only, as integers: for 8-bit
+ * samples two 16-bit lanes per register (k * 255 < 2^16), columns (0, 2) and
+ * (1, 3) of each 4-byte word; for 16-bit samples one register per column, or
+ * two 16-bit lanes per word when k * (2^bitdepth - 1) < 2^16 (packed16).
+ * Inexact taps: sample sums and product errors as fp32 pairs of adjacent
+ * columns (both exact: integers below 2^24, and multiples of 2^-E below
+ * 2^24 * 2^-E). */
 template <typename T, bool kExactTap>
 struct ColAcc {
     static constexpr int V = 16 / sizeof(T);
     unsigned s[8];
-    float e[V];
+    float2 sx[V / 2];
+    float2 ex[V / 2];
 
     __device__ __forceinline__ void reset()
     {
+        if constexpr (kExactTap) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-            s[i] = 0u;
+            for (int i = 0; i < 8; ++i)
+                s[i] = 0u;
+        } else {
 #pragma unroll
-        for (int v = 0; v < V; ++v)
-            e[v] = 0.0f;
+            for (int j = 0; j < V / 2; ++j) {
+                sx[j] = make_float2(0.0f, 0.0f);
+                ex[j] = make_float2(0.0f, 0.0f);
+            }
+        }
     }
 
-    /* fp32 value of sample v of the 16-byte vector (exact: 2^23 + s - 2^23) */
-    __device__ __forceinline__ static float sample_f(const uint4 &q, int v)
+    /* bits of 2^23 + sample v of the 16-byte vector, as fp32 */
+    __device__ __forceinline__ static float magic(const uint4 &q, int v)
     {
         const unsigned w = v < V / 4 ? q.x : v < V / 2 ? q.y
                                    : v < 3 * V / 4 ? q.z : q.w;
@@ -122,36 +170,41 @@ struct ColAcc {
             bits = __byte_perm(w, 0x4B000000u, 0x7540u | (unsigned)(v & 3));
         else
             bits = __byte_perm(w, 0x4B000000u, (v & 1) ? 0x7432u : 0x7410u);
-        return __fsub_rn(__uint_as_float(bits), 8388608.0f);
+        return __uint_as_float(bits);
     }
 
     __device__ __forceinline__ void add(const uint4 &q, bool packed16,
-                                        float tap)
+                                        const PairConsts &c)
     {
-        const unsigned w[4] = {q.x, q.y, q.z, q.w};
-        if (sizeof(T) == 1) {
+        if constexpr (kExactTap) {
+            const unsigned w[4] = {q.x, q.y, q.z, q.w};
+            if (sizeof(T) == 1) {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                s[2 * j] += __byte_perm(w[j], 0u, 0x4240u);
-                s[2 * j + 1] += __byte_perm(w[j], 0u, 0x4341u);
+                for (int j = 0; j < 4; ++j) {
+                    s[2 * j] += __byte_perm(w[j], 0u, 0x4240u);
+                    s[2 * j + 1] += __byte_perm(w[j], 0u, 0x4341u);
+                }
+            } else if (packed16) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    s[j] += w[j];
+            } else {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    s[2 * j] += w[j] & 0xffffu;
+                    s[2 * j + 1] += w[j] >> 16;
+                }
             }
-        } else if (packed16) {
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-                s[j] += w[j];
         } else {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                s[2 * j] += w[j] & 0xffffu;
-                s[2 * j + 1] += w[j] >> 16;
-            }
-        }
-        if (!kExactTap) {
-#pragma unroll
-            for (int v = 0; v < V; ++v) {
-                const float xf = sample_f(q, v);
-                const float prod = __fmul_rn(xf, tap);
-                e[v] = __fadd_rn(e[v], __fmaf_rn(xf, tap, -prod));
+            for (int j = 0; j < V / 2; ++j) {
+                const float2 mb = make_float2(magic(q, 2 * j),
+                                              magic(q, 2 * j + 1));
+                const float2 x = fma2_rn(mb, c.one, c.m23);       // exact
+                const float2 nprod = mul2_rn(x, c.ntap);          // -fl(x t)
+                const float2 e = fma2_rn(x, c.tap, nprod);        // exact
+                ex[j] = fma2_rn(e, c.one, ex[j]);
+                sx[j] = fma2_rn(x, c.one, sx[j]);
             }
         }
     }
@@ -159,15 +212,19 @@ struct ColAcc {
     /* sample sum of column v */
     __device__ __forceinline__ int col(int v, bool packed16) const
     {
-        if (sizeof(T) == 1) {
-            const unsigned r = s[2 * (v >> 2) + (v & 1)];
-            return (int)((v & 2) ? r >> 16 : r & 0xffffu);
+        if constexpr (!kExactTap) {
+            return __float2int_rn((v & 1) ? sx[v >> 1].y : sx[v >> 1].x);
+        } else {
+            if (sizeof(T) == 1) {
+                const unsigned r = s[2 * (v >> 2) + (v & 1)];
+                return (int)((v & 2) ? r >> 16 : r & 0xffffu);
+            }
+            if (packed16) {
+                const unsigned r = s[v >> 1];
+                return (int)((v & 1) ? r >> 16 : r & 0xffffu);
+            }
+            return (int)s[v];
         }
-        if (packed16) {
-            const unsigned r = s[v >> 1];
-            return (int)((v & 1) ? r >> 16 : r & 0xffffu);
-        }
-        return (int)s[v];
     }
 
     /* write the V column sums of group g to one output row's arrays */
@@ -178,9 +235,10 @@ struct ColAcc {
 #pragma unroll
         for (int v = 0; v < V; ++v) {
             rowS[base + v] = col(v, packed16);
-            if (!kExactTap)
-                rowE[base + v] =
-                    __float2int_rn(__fmul_rn(e[v], err_scale));
+            if constexpr (!kExactTap) {
+                const float e = (v & 1) ? ex[v >> 1].y : ex[v >> 1].x;
+                rowE[base + v] = __float2int_rn(__fmul_rn(e, err_scale));
+            }
         }
     }
 };
@@ -244,6 +302,10 @@ ssim_decimate_kernel(const DecimateParams p)
     const int Ca = kVec ? (C0 & ~(V - 1)) : C0;
     const int G = (C1 + 1 - Ca + V - 1) / V;
 
+    const PairConsts pc = {p.one2, make_float2(-8388608.0f, -8388608.0f),
+                           make_float2(p.tap, p.tap),
+                           make_float2(-p.tap, -p.tap)};
+
     /* Phase 1: thread (g, sub) sums column group g over the k input rows of
      * output rows sub, sub + m, sub + 2m, ... */
     const int m = kThreads / G > 0 ? kThreads / G : 1;
@@ -275,7 +337,7 @@ ssim_decimate_kernel(const DecimateParams p)
                     if (rb + b < nr) {
 #pragma unroll
                         for (int i = 0; i < (K > 0 ? K : 1); ++i)
-                            acc.add(q[b][i], p.packed16, p.tap);
+                            acc.add(q[b][i], p.packed16, pc);
                         const int r = sub + (rb + b) * m;
                         acc.store(sS + r * p.pitch, sE + r * p.pitch, g,
                                   p.packed16, p.err_scale);
@@ -314,7 +376,7 @@ ssim_decimate_kernel(const DecimateParams p)
                         ++ri;
                     }
                     if (u0 + j < total) {
-                        acc.add(q[j], p.packed16, p.tap);
+                        acc.add(q[j], p.packed16, pc);
                         if (row_end) {
                             acc.store(sS + r * p.pitch, sE + r * p.pitch, g,
                                       p.packed16, p.err_scale);
