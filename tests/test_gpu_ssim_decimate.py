@@ -244,3 +244,27 @@ def test_8bit_partials_with_unaligned_outputs(fv):
                               o[0].ravel().view(np.uint32))
         assert np.array_equal(big_d[1:].cpu().numpy().view(np.uint32),
                               o[1].ravel().view(np.uint32))
+
+
+@pytest.mark.parametrize("bitdepth,scale,w,h", [
+    (8, 2, 1920, 9), (8, 3, 1600, 10), (8, 5, 3840, 11), (8, 6, 2560, 13),
+    (8, 7, 3600, 15), (10, 2, 8192, 5), (10, 3, 3840, 7), (10, 4, 1920, 9),
+    (10, 5, 800, 12), (12, 6, 1536, 13), (16, 7, 1792, 15), (16, 8, 3840, 17),
+    (8, 3, 48, 7), (16, 2, 16, 16),
+])
+@pytest.mark.parametrize("kernel", ["auto", "general", "windows"])
+def test_window_kernel_chunk_boundaries(fv, monkeypatch, kernel, bitdepth,
+                                        scale, w, h):
+    """Rows of a multiple of 16 bytes at scales 2..8 take the window kernel
+    (or, where it measures faster, the general one; FSSIM_KERNEL forces
+    either, and both must give the oracle's bits):
+    chunks of 16 k bytes, the neighbour's half window by shuffle, lane 0 of
+    later warps and the first chunk of a second block column loading the
+    previous chunk's last vector, the mirrored first window, a partial last
+    chunk, top-of-range samples."""
+    monkeypatch.setenv("FSSIM_KERNEL", kernel)
+    rng = np.random.default_rng(w * 7 + scale)
+    for mode in ("random", "top"):
+        ref = rand_frames(rng, 2, h, w, bitdepth, mode)
+        dist = rand_frames(rng, 2, h, w, bitdepth, mode)
+        check(fv, ref, dist, bitdepth, scale)

@@ -9,11 +9,29 @@
  */
 #include <cmath>
 #include <cstdint>
+#include <cstdlib>
+#include <cstring>
 
 #include "../../include/fssim.h"
 #include "fssim_kernels.cuh"
 
 using namespace fssim;
+
+namespace fssim {
+
+FixedPath fixed_path_override()
+{
+    const char *v = std::getenv("FSSIM_KERNEL");
+    if (!v)
+        return FixedPath::kAuto;
+    if (std::strcmp(v, "general") == 0)
+        return FixedPath::kGeneral;
+    if (std::strcmp(v, "windows") == 0)
+        return FixedPath::kWindows;
+    return FixedPath::kAuto;
+}
+
+} // namespace fssim
 
 namespace {
 

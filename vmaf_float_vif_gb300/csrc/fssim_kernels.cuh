@@ -549,6 +549,184 @@ ssim_decimate_u8_partials_kernel(const DecimateParams p)
     }
 }
 
+/* Any k in 2..8, 8- or 16-bit samples, rows a multiple of 16 bytes: each
+ * thread owns a chunk of 16k bytes (NS = WT * k samples, WT = 16 windows for
+ * 8-bit samples, 8 for 16-bit) and loads it as k 16-byte vectors per input
+ * row.  Chunk column c belongs to window (c + k/2) / k of the chunk: window 0
+ * is the right half of a window that starts in the previous chunk, windows
+ * 1..WT-1 lie inside, window WT is the left part of the next chunk's window
+ * 0.  All window indices and byte masks are compile-time constants, so the
+ * sample sums go straight into per-window registers with dp4a (bytes) or
+ * dp2a (16-bit halves), and the product errors (inexact taps) into
+ * per-window fp32 sums from packed fp32 pairs.  Window 0 adds the left
+ * neighbour's window WT (shuffle from lane - 1); lane 0 of a warp and the
+ * first chunk of a block column load the previous chunk's last vector with
+ * their own rows, and chunk 0 mirrors its first k/2 columns.  The last
+ * window of a row never leaves the row (w even), so the right edge needs no
+ * mirror.  No shared memory, no barrier. */
+template <typename T, int K>
+__global__ void __launch_bounds__(kThreads)
+ssim_decimate_windows_kernel(const DecimateParams p)
+{
+    static_assert(K >= 2 && K <= 8, "window kernel for k = 2..8");
+    constexpr bool kExact = (K & (K - 1)) == 0;
+    constexpr int V = 16 / sizeof(T);     // samples per 16-byte vector
+    constexpr int WT = V;                 // windows per chunk
+    constexpr int NS = WT * K;            // samples per chunk
+    constexpr int H = K / 2;
+    constexpr int SPW = 4 / sizeof(T);    // samples per 32-bit word
+    const int plane = blockIdx.z & 1;
+    const size_t f = blockIdx.z >> 1;
+    const T *src = static_cast<const T *>(plane ? p.src[1] : p.src[0]) +
+                   f * p.in_frame_elems;
+    float *dst = (plane ? p.dst[1] : p.dst[0]) + f * p.out_frame_elems;
+    const int w = p.w, h = p.h;
+    const int G = (p.sw + WT - 1) / WT;   // chunks per row
+    const int Gb = p.X;                   // chunks per block column
+    const int m = kThreads / Gb;
+    const int t = threadIdx.x;
+    const int gi = t % Gb;
+    const int sub = t / Gb;
+    const int g = blockIdx.x * Gb + gi;
+    const bool col_ok = sub < m && g < G;
+    const int lane = t & 31;
+    const bool nb_in_warp = lane > 0 && gi > 0;
+    const bool need_prev = !nb_in_warp && g > 0;
+    const int y0 = blockIdx.y * p.R;
+    const int rn = min(p.R, p.sh - y0);
+    const int iters = (p.R + m - 1) / m;
+    const T *chunk = src + (size_t)NS * g;
+    /* vectors of this chunk inside the row (w is a multiple of V) */
+    const int nvec = min(K, (w - NS * g) / V);
+    const float2 one = p.one2;
+    const float2 m23 = make_float2(-8388608.0f, -8388608.0f);
+    const float2 tap2 = make_float2(p.tap, p.tap);
+    const float2 ntap2 = make_float2(-p.tap, -p.tap);
+
+    for (int it = 0; it < iters; ++it) {
+        const int r = sub + it * m;
+        const bool act = col_ok && r < rn;
+        const int yb = K * (y0 + r) - H;
+        unsigned S[WT + 1];
+        float E[WT + 1];
+#pragma unroll
+        for (int i = 0; i <= WT; ++i) {
+            S[i] = 0u;
+            E[i] = 0.0f;
+        }
+        unsigned Sp = 0u;                 // previous chunk's window WT, or
+        float Ep = 0.0f;                  // the mirror of this chunk's start
+        if (act) {
+            for (int i = 0; i < K; ++i) {
+                const T *rp = chunk + (size_t)mirror2n(yb + i, h) * w;
+                uint4 q[K];
+                uint4 qp = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+                for (int v = 0; v < K; ++v)
+                    q[v] = v < nvec
+                               ? __ldg(reinterpret_cast<const uint4 *>(rp) + v)
+                               : make_uint4(0u, 0u, 0u, 0u);
+                if (need_prev)
+                    qp = __ldg(reinterpret_cast<const uint4 *>(rp) - 1);
+#pragma unroll
+                for (int v = 0; v < K; ++v) {
+                    const unsigned wd[4] = {q[v].x, q[v].y, q[v].z, q[v].w};
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int c0 = V * v + SPW * j;   // first sample
+                        const int wa = (c0 + H) / K;
+                        /* sample sums: the word's samples of window wa..wa+2 */
+#pragma unroll
+                        for (int dw = 0; dw < 3; ++dw) {
+                            const int win = wa + dw;
+                            /* dp4a: byte b of the mask weighs byte b of the
+                             * word; dp2a_lo: bytes 0 and 1 of the mask weigh
+                             * the word's two 16-bit halves */
+                            unsigned msk = 0u;
+#pragma unroll
+                            for (int b = 0; b < SPW; ++b)
+                                if ((c0 + b + H) / K == win)
+                                    msk |= 1u << (8 * b);
+                            if (win <= WT && msk != 0u) {
+                                if constexpr (sizeof(T) == 1)
+                                    S[win] = __dp4a(wd[j], msk, S[win]);
+                                else
+                                    S[win] = __dp2a_lo(wd[j], msk, S[win]);
+                            }
+                        }
+                        if constexpr (!kExact) {
+#pragma unroll
+                            for (int pp = 0; pp < SPW / 2; ++pp) {
+                                const int c = c0 + 2 * pp;
+                                const float2 x = fma2_rn(
+                                    make_float2(
+                                        ColAcc<T, false>::magic(q[v], c - V * v),
+                                        ColAcc<T, false>::magic(q[v],
+                                                                c + 1 - V * v)),
+                                    one, m23);
+                                const float2 e = fma2_rn(
+                                    x, tap2, mul2_rn(x, ntap2));
+                                const int w0 = (c + H) / K;
+                                const int w1 = (c + 1 + H) / K;
+                                E[w0] = __fadd_rn(E[w0], e.x);
+                                E[w1] = __fadd_rn(E[w1], e.y);
+                            }
+                        }
+                    }
+                }
+                /* the samples outside this chunk that window 0 needs */
+                if (need_prev || g == 0) {
+                    const uint4 qs = need_prev ? qp : q[0];
+#pragma unroll
+                    for (int b = 0; b < H; ++b) {
+                        const int c = need_prev ? V - H + b : b;
+                        const unsigned wv = c < V / 4 ? qs.x
+                                          : c < V / 2 ? qs.y
+                                          : c < 3 * V / 4 ? qs.z : qs.w;
+                        const unsigned sv =
+                            sizeof(T) == 1 ? (wv >> (8 * (c & 3))) & 0xffu
+                                           : (wv >> (16 * (c & 1))) & 0xffffu;
+                        Sp += sv;
+                        if constexpr (!kExact) {
+                            const float xf = (float)sv;
+                            const float pr = __fmul_rn(xf, p.tap);
+                            Ep = __fadd_rn(Ep, __fmaf_rn(xf, p.tap, -pr));
+                        }
+                    }
+                }
+            }
+        }
+        const unsigned s_left = __shfl_up_sync(0xffffffffu, S[WT], 1);
+        const float e_left = __shfl_up_sync(0xffffffffu, E[WT], 1);
+        if (act) {
+            if (nb_in_warp) {
+                Sp = s_left;
+                Ep = e_left;
+            }
+            float *orow = dst + (size_t)(y0 + r) * p.sw + WT * g;
+            const int nout = min(WT, p.sw - WT * g);
+#pragma unroll
+            for (int i = 0; i < WT; ++i) {
+                if (i < nout) {
+                    const unsigned Sw = i == 0 ? S[0] + Sp : S[i];
+                    float o;
+                    if constexpr (kExact) {
+                        o = __fmul_rn(__uint2float_rn(Sw), p.out_scale);
+                    } else {
+                        const float Ew = i == 0 ? __fadd_rn(E[0], Ep) : E[i];
+                        const long long n =
+                            p.T * (long long)Sw -
+                            (long long)__float2int_rn(
+                                __fmul_rn(Ew, p.err_scale));
+                        o = __fmul_rn(__ll2float_rn(n), p.out_scale);
+                    }
+                    orow[i] = o;
+                }
+            }
+        }
+    }
+}
+
 /* Scale 1: the converted samples. */
 template <typename T>
 __global__ void __launch_bounds__(kThreads)
@@ -621,13 +799,64 @@ cudaError_t launch_partials(DecimateParams p, int n_frames,
     return cudaSuccess;
 }
 
+/* Launch shape of the window kernel: p.X chunks per block column, p.R output
+ * rows per block. */
+template <typename T, int K>
+cudaError_t launch_windows(DecimateParams p, int n_frames,
+                           cudaStream_t stream)
+{
+    constexpr int WT = 16 / sizeof(T);
+    const int G = (p.sw + WT - 1) / WT;
+    p.X = G < kThreads ? G : kThreads;
+    const int m = kThreads / p.X;
+    p.R = 2 * m < p.sh ? 2 * m : p.sh;
+    DecimateParams q = p;
+    const size_t in_bytes = p.in_frame_elems * sizeof(T);
+    for (int f0 = 0; f0 < n_frames; f0 += kMaxFramesPerLaunch) {
+        const int nf = n_frames - f0 < kMaxFramesPerLaunch
+                           ? n_frames - f0 : kMaxFramesPerLaunch;
+        for (int s = 0; s < 2; ++s) {
+            q.src[s] = static_cast<const unsigned char *>(p.src[s]) +
+                       in_bytes * (size_t)f0;
+            q.dst[s] = p.dst[s] + p.out_frame_elems * (size_t)f0;
+        }
+        const dim3 grid((G + p.X - 1) / p.X, (p.sh + p.R - 1) / p.R, 2 * nf);
+        ssim_decimate_windows_kernel<T, K><<<grid, kThreads, 0, stream>>>(q);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess)
+            return e;
+    }
+    return cudaSuccess;
+}
+
+/* Which kernel takes a fixed scale on the vector path: the window kernel or
+ * the general two-phase one (measured choice per sample type and scale;
+ * FSSIM_KERNEL=general or =windows in the environment overrides it). */
+enum class FixedPath { kAuto, kGeneral, kWindows };
+FixedPath fixed_path_override();
+
+template <typename T, int K>
+constexpr bool prefer_windows()
+{
+    /* measured at 4K: the general kernel's coalesced loads win for 8-bit
+     * samples at k = 2 and 16-bit samples at k = 8 */
+    return !(sizeof(T) == 1 && K == 2) && !(sizeof(T) == 2 && K == 8);
+}
+
 template <typename T, int K>
 cudaError_t launch_fixed(const DecimateParams &p, bool vec, int n_frames,
                          size_t smem, cudaStream_t stream)
 {
     constexpr bool kExact = (K & (K - 1)) == 0;
-    return vec ? launch<T, K, kExact, true>(p, n_frames, smem, stream)
-               : launch<T, K, kExact, false>(p, n_frames, smem, stream);
+    if (vec) {
+        const FixedPath o = fixed_path_override();
+        const bool windows = o == FixedPath::kAuto ? prefer_windows<T, K>()
+                                                   : o == FixedPath::kWindows;
+        if (windows)
+            return launch_windows<T, K>(p, n_frames, stream);
+        return launch<T, K, kExact, true>(p, n_frames, smem, stream);
+    }
+    return launch<T, K, kExact, false>(p, n_frames, smem, stream);
 }
 
 /* All kernels for one sample type (defined in fssim_u8.cu / fssim_u16.cu). */
