@@ -798,10 +798,14 @@ int fvif_score_host(fvif_ctx *ctx, const void *ref, const void *dist,
     const size_t pb = ctx->plane_bytes();
     const size_t half = pb * (size_t)ctx->chunk;
     cudaError_t e = fork_lanes(ctx);
+    /* The first chunk is a quarter chunk: scoring starts once it has been
+     * copied instead of waiting for a whole chunk to cross the host link. */
+    const int first = ctx->chunk >= 4 ? ctx->chunk / 4 : ctx->chunk;
     int i = 0;
-    for (int f0 = 0; f0 < n_frames && e == cudaSuccess; f0 += ctx->chunk, ++i) {
-        const int nf = (n_frames - f0 < ctx->chunk) ? n_frames - f0
-                                                    : ctx->chunk;
+    for (int f0 = 0, nf = 0; f0 < n_frames && e == cudaSuccess;
+         f0 += nf, ++i) {
+        const int want = i == 0 ? first : ctx->chunk;
+        nf = (n_frames - f0 < want) ? n_frames - f0 : want;
         /* chunk i is copied into staging slot i % slots while earlier
          * chunks are scored, and scored on lane i % lanes */
         const int slot = i % ctx->stage_slots;
