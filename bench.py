@@ -55,6 +55,7 @@ WORKLOADS = {
     "c4_4k_8b": ("c4_4k_8b", 20, 1.0),
     "c2_1080p_10b": ("c2_checker_1px_10b", 240, 1.0),
     "c3_1080p_16b": ("c3_bright_1080p_16b", 240, 1.0),
+    "c1_576x324_8b": ("c1_576x324_8b", 960, 1.0),
 }
 
 
@@ -204,9 +205,12 @@ def kernel_hash():
     return h.hexdigest()[:16]
 
 
-def load_traffic(workload):
-    """Per-launch DRAM bytes of the scale-0 statistic kernel from a committed
-    ncu summary, only if it was taken on the current kernel sources."""
+def load_traffic(workload, frames_per_launch):
+    """DRAM bytes of one scale-0 statistic launch of frames_per_launch frames,
+    from a committed ncu summary taken on the current kernel sources.  The
+    capture holds fewer frames than a full launch; the traffic of a launch
+    grows in proportion to its frames (each frame is read once), so it is
+    scaled by the frame count."""
     try:
         with open(TRAFFIC_PATH) as f:
             t = json.load(f)
@@ -214,7 +218,11 @@ def load_traffic(workload):
         return None
     if t.get("kernel_hash") != kernel_hash():
         return None
-    return t.get("per_launch_bytes", {}).get(workload)
+    b = t.get("per_launch_bytes", {}).get(workload)
+    n = t.get("frames_per_launch")
+    if b is None or not n:
+        return None
+    return b * frames_per_launch / n
 
 
 def host_link_gbs(copies: int = 8):
@@ -427,11 +435,15 @@ def run_ours(args):
     st0_ms, st0_n = prof["stats_scale0"]
     launches_total = sum(n for _, n in prof.values())
     px0 = case.w * case.h
-    ops_launch = chunk * px0 * stats_ops_per_pixel(n0)
+    # frames per scale-0 launch: full chunks, the last one partial
+    launches_step = -(-frames // chunk)
+    frames_launch = frames / launches_step
+    ops_launch = frames_launch * px0 * stats_ops_per_pixel(n0)
+    ops_solo = n_solo * px0 * stats_ops_per_pixel(n0)
     avg_ms = st0_ms / max(1, st0_n)
     achieved = ops_launch / (avg_ms / 1e3) / 1e12
     alu_peak = SMS * FP32_LANES_PER_SM * sm_max * 1e6 / 1e12
-    traffic = load_traffic(args.workload)
+    traffic = load_traffic(args.workload, frames_launch)
     kernel_shares = {k: {"ms": v[0], "launches": v[1],
                          "share": v[0] / max(1e-9, sum(x[0] for x in
                                                        prof.values()))}
@@ -464,8 +476,8 @@ def run_ours(args):
             "kernels": kernel_shares,
         },
         "roofline": {
-            "kernel": "stats_kernel, scale 0 (%d taps), %d frames per launch"
-                      % (n0, chunk),
+            "kernel": "stats_kernel, scale 0 (%d taps), %.4g frames per "
+                      "launch (chunks of %d)" % (n0, frames_launch, chunk),
             "bound": "alu",
             "achieved": achieved,
             "peak": alu_peak,
@@ -484,8 +496,8 @@ def run_ours(args):
                            "run on two streams, so a launch shares the GPU "
                            "with the other chunk's smaller kernels",
             "solo_launch_ms": solo_ms,
-            "solo_achieved": ops_launch / (solo_ms / 1e3) / 1e12,
-            "solo_frac": ops_launch / (solo_ms / 1e3) / 1e12 / alu_peak,
+            "solo_achieved": ops_solo / (solo_ms / 1e3) / 1e12,
+            "solo_frac": ops_solo / (solo_ms / 1e3) / 1e12 / alu_peak,
             "solo_note": "the same launch with no other chunk in flight "
                          "(one 16-frame chunk scored alone after the timed "
                          "region, events on its stream)",

@@ -144,7 +144,10 @@ int fvif_last_error(const fvif_ctx *ctx);
 /* Static text for a status code. */
 const char *fvif_strerror(int status);
 
-/* Number of frames the context scores per chunk. */
+/* Number of frames the context scores per chunk of device inputs: enough
+ * frames for about 4096 scale-0 strips of 16 rows per launch, at least 16
+ * (31 at 3840x2160, 61 at 1920x1080).  fvif_score_host streams host inputs
+ * in chunks of at most 16 frames. */
 int fvif_chunk_frames(const fvif_ctx *ctx);
 
 /* Copy the fp32 taps of scale s (0..3) into taps[0..cap); returns the tap

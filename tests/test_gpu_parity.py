@@ -76,19 +76,21 @@ def c5_stream():
 @pytest.mark.parametrize("ks", [0.5, 1.0, 2.0])
 def test_4k_10bit_stream_sampled(fv, ks):
     """The 240-frame 10-bit 4K stream in the benchmark's launch
-    configuration (device inputs, one fvif_score_async call, chunks of 16);
-    sampled frames against the oracle."""
+    configuration (device inputs, one fvif_score_async call, the context's
+    default chunk: about 4096 scale-0 strips per launch, 31 frames at 4K);
+    sampled frames on both sides of chunk boundaries against the oracle."""
     torch = torch_mod()
     case = S.CASES["c5_4k_10b"]
     ref, dist = c5_stream()
     r, d = to_device(ref), to_device(dist)
     out = torch.empty(4 * case.frames, dtype=torch.float64, device="cuda")
     with fv.Context(case.w, case.h, case.bitdepth, ks, case.nsq) as ctx:
-        assert ctx.chunk_frames == 16
+        strips = (case.h + 15) // 16
+        assert ctx.chunk_frames == max(16, -(-4096 // strips)) == 31
         ctx.score_async(r, d, out)
         torch.cuda.synchronize()
     got = out.cpu().numpy().reshape(-1, 4)
-    samples = [0, 17, 128, 239]
+    samples = [0, 17, 30, 31, 128, 239]
     want = oracle_scores(ref[samples], dist[samples], 10, ks, case.nsq)
     assert_bitwise(got[samples], want, "c5 ks=%g" % ks)
     assert np.all((got > 0) & (got <= 1.0 + 1e-6))

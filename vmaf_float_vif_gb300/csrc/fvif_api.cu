@@ -16,7 +16,9 @@ using namespace fvif;
 
 namespace {
 
-constexpr int kDefaultChunk = 16;
+constexpr int kDefaultChunk = 16;   /* smallest chunk, in frames       */
+constexpr int kMaxChunk = 1024;     /* largest chunk, in frames        */
+constexpr int kChunkCtas = 4096;    /* scale-0 CTAs per chunk wanted   */
 constexpr int kLanes = 2; /* chunks alternate between two streams */
 constexpr int kMaxStage = 4; /* host-input staging slots, at most */
 
@@ -128,6 +130,10 @@ struct fvif_ctx {
     int ws[kScales] = {}, hs[kScales] = {};
     Taps taps[kScales];
     int chunk = kDefaultChunk;
+    /* frames per chunk of the host-input path (staging slot size): at most
+     * kDefaultChunk, which measured fastest there (finer copy/score
+     * interleaving), whatever the device-input chunk */
+    int host_chunk = kDefaultChunk;
     int device = 0;
     cudaStream_t stream = nullptr;
     int last_status = FVIF_OK;
@@ -469,7 +475,7 @@ int ensure_pipeline(fvif_ctx *c)
 {
     if (c->copy_stream)
         return FVIF_OK;
-    const size_t slot = 2 * c->plane_bytes() * (size_t)c->chunk;
+    const size_t slot = 2 * c->plane_bytes() * (size_t)c->host_chunk;
     cudaError_t e = cudaStreamCreateWithFlags(&c->copy_stream,
                                               cudaStreamNonBlocking);
     for (int i = 0; i < c->stage_slots && e == cudaSuccess; ++i) {
@@ -559,11 +565,21 @@ fvif_ctx *fvif_create_ex(int w, int h, int bitdepth, float kernelscale,
             return nullptr;
         }
     }
+    /* Frames per chunk: enough that the scale-0 statistic launch has about
+     * kChunkCtas CTAs (one per 16-row strip and frame; measured best for
+     * 576x324, 1080p and 4K alike), at least kDefaultChunk frames. */
+    {
+        const int strips = (h + 15) / 16;
+        int v = (kChunkCtas + strips - 1) / strips;
+        v = v < kDefaultChunk ? kDefaultChunk : (v > kMaxChunk ? kMaxChunk : v);
+        c->chunk = v;
+    }
     if (const char *env = std::getenv("FVIF_CHUNK")) {
         const int v = std::atoi(env);
-        if (v > 0 && v <= 256)
+        if (v > 0 && v <= kMaxChunk)
             c->chunk = v;
     }
+    c->host_chunk = c->chunk < kDefaultChunk ? c->chunk : kDefaultChunk;
     if (const char *env = std::getenv("FVIF_HOST_SLOTS")) {
         const int v = std::atoi(env);
         if (v >= 2 && v <= kMaxStage)
@@ -796,15 +812,16 @@ int fvif_score_host(fvif_ctx *ctx, const void *ref, const void *dist,
      * the host frames may be further apart (frame_stride) */
     const size_t fb = ctx->frame_bytes();
     const size_t pb = ctx->plane_bytes();
-    const size_t half = pb * (size_t)ctx->chunk;
+    const int hc = ctx->host_chunk;
+    const size_t half = pb * (size_t)hc;
     cudaError_t e = fork_lanes(ctx);
     /* The first chunk is a quarter chunk: scoring starts once it has been
      * copied instead of waiting for a whole chunk to cross the host link. */
-    const int first = ctx->chunk >= 4 ? ctx->chunk / 4 : ctx->chunk;
+    const int first = hc >= 4 ? hc / 4 : hc;
     int i = 0;
     for (int f0 = 0, nf = 0; f0 < n_frames && e == cudaSuccess;
          f0 += nf, ++i) {
-        const int want = i == 0 ? first : ctx->chunk;
+        const int want = i == 0 ? first : hc;
         nf = (n_frames - f0 < want) ? n_frames - f0 : want;
         /* chunk i is copied into staging slot i % slots while earlier
          * chunks are scored, and scored on lane i % lanes */
