@@ -31,6 +31,17 @@
  *  - A context is not thread-safe; separate contexts are independent.
  *  - All work runs on the context's CUDA stream (default: the legacy default
  *    stream; see fvif_set_stream).
+ *
+ * Environment variables read by the library (none is needed):
+ *  - FVIF_LOG: when set, one line per create and score call on stderr (size,
+ *    frames, chunk, status, host wall time; for fvif_score_async the time to
+ *    enqueue).
+ *  - FVIF_CHUNK=n: frames per chunk of device inputs (1..1024) instead of
+ *    the default, read by fvif_create.
+ *  - FVIF_FAIL_ALLOC=n: test hook, read by fvif_create: allocation n
+ *    (0 = the first) of the context fails as if the device were out of
+ *    memory, so every failure path can be exercised without exhausting
+ *    device memory.
  */
 #ifndef FVIF_H
 #define FVIF_H

@@ -4,6 +4,7 @@ invalid arguments before any CUDA call."""
 import ctypes
 import os
 import re
+import sys
 import subprocess
 
 import pytest
@@ -172,3 +173,26 @@ def test_ssim_decimate_rejects_null_and_misaligned_buffers(L):
                             None) == fv.FVIF_OK
     assert L.fssim_decimate(16, 16, 8, 128, p, p, 1, p, p, None) == \
         fv.FVIF_OK
+
+
+def test_fvif_log_lines_for_rejected_calls(L):
+    """FVIF_LOG prints one line per call, with its status, even for calls
+    rejected before any CUDA work (no GPU needed)."""
+    code = (
+        "import ctypes, vmaf_float_vif_gb300 as fv\n"
+        "L = fv.lib()\n"
+        "assert not L.fvif_create(8, 8, 8, 1.0, 2.0)\n"
+        "assert L.fvif_score(None, None, None, 1, None) == fv.FVIF_EINVAL\n")
+    env = dict(os.environ, FVIF_LOG="1")
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env,
+                       capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stderr
+    lines = [x for x in r.stderr.splitlines() if x.startswith("fvif: ")]
+    assert any(x.startswith("fvif: create 8x8 bitdepth=8") and
+               "status=-1" in x for x in lines), r.stderr
+    assert any(x.startswith("fvif: score 0x0 frames=1") and
+               "status=-1" in x for x in lines), r.stderr
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT,
+                       env={k: v for k, v in env.items() if k != "FVIF_LOG"},
+                       capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0 and "fvif: " not in r.stderr

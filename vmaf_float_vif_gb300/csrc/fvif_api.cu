@@ -3,6 +3,7 @@
  * the C ABI declared in include/fvif.h.
  */
 #include <cmath>
+#include <chrono>
 #include <cstdio>
 #include <vector>
 #include <cstdlib>
@@ -134,6 +135,10 @@ struct fvif_ctx {
      * kDefaultChunk, which measured fastest there (finer copy/score
      * interleaving), whatever the device-input chunk */
     int host_chunk = kDefaultChunk;
+    /* test hook (FVIF_FAIL_ALLOC=n): allocation number n of this context
+     * (0 = the first) fails as if the device were out of memory */
+    int fail_alloc_at = -1;
+    int allocs = 0;
     int device = 0;
     cudaStream_t stream = nullptr;
     int last_status = FVIF_OK;
@@ -198,6 +203,42 @@ int cuda_status(cudaError_t e)
     return FVIF_ECUDA;
 }
 
+/* Every device or pinned-host allocation of a context goes through these,
+ * so the allocation-failure hook can fail any one of them. */
+cudaError_t ctx_malloc(fvif_ctx *c, void **p, size_t n)
+{
+    if (c->allocs++ == c->fail_alloc_at)
+        return cudaErrorMemoryAllocation;
+    return cudaMalloc(p, n);
+}
+
+cudaError_t ctx_malloc_host(fvif_ctx *c, void **p, size_t n)
+{
+    if (c->allocs++ == c->fail_alloc_at)
+        return cudaErrorMemoryAllocation;
+    return cudaMallocHost(p, n);
+}
+
+/* The host-input pipeline (staging slots, their events, the copy stream);
+ * leaves the context as if no pipeline had been made. */
+void release_pipeline(fvif_ctx *c)
+{
+    for (int i = 0; i < kMaxStage; ++i) {
+        if (c->stage[i])
+            cudaFree(c->stage[i]);
+        if (c->copied[i])
+            cudaEventDestroy(c->copied[i]);
+        if (c->consumed[i])
+            cudaEventDestroy(c->consumed[i]);
+        c->stage[i] = nullptr;
+        c->copied[i] = nullptr;
+        c->consumed[i] = nullptr;
+    }
+    if (c->copy_stream)
+        cudaStreamDestroy(c->copy_stream);
+    c->copy_stream = nullptr;
+}
+
 void release(fvif_ctx *c)
 {
     for (fvif_ctx::Lane &l : c->lanes) {
@@ -225,16 +266,7 @@ void release(fvif_ctx *c)
         cudaFree(c->d_debug);
     if (c->h_debug)
         cudaFreeHost(c->h_debug);
-    for (int i = 0; i < kMaxStage; ++i) {
-        if (c->stage[i])
-            cudaFree(c->stage[i]);
-        if (c->copied[i])
-            cudaEventDestroy(c->copied[i]);
-        if (c->consumed[i])
-            cudaEventDestroy(c->consumed[i]);
-    }
-    if (c->copy_stream)
-        cudaStreamDestroy(c->copy_stream);
+    release_pipeline(c);
     for (int k = 0; k < FVIF_K_COUNT; ++k)
         for (cudaEvent_t ev : c->prof_events[k])
             cudaEventDestroy(ev);
@@ -407,9 +439,11 @@ int ensure_out(fvif_ctx *c, int n)
     while (cap < n)
         cap *= 2;
     double *d = nullptr, *h = nullptr;
-    if (cudaMalloc(&d, sizeof(double) * kScales * (size_t)cap) != cudaSuccess)
+    if (ctx_malloc(c, (void **)&d, sizeof(double) * kScales * (size_t)cap) !=
+        cudaSuccess)
         return FVIF_ENOMEM;
-    if (cudaMallocHost(&h, sizeof(double) * kScales * (size_t)cap) !=
+    if (ctx_malloc_host(c, (void **)&h,
+                        sizeof(double) * kScales * (size_t)cap) !=
         cudaSuccess) {
         cudaFree(d);
         return FVIF_ENOMEM;
@@ -433,11 +467,13 @@ int ensure_debug(fvif_ctx *c, int n)
         cap *= 2;
     float2 *sm = nullptr;
     double *d = nullptr, *h = nullptr;
-    cudaError_t e = cudaMalloc(&sm, sizeof(float2) * kScales * (size_t)cap);
+    cudaError_t e = ctx_malloc(c, (void **)&sm,
+                               sizeof(float2) * kScales * (size_t)cap);
     if (e == cudaSuccess)
-        e = cudaMalloc(&d, sizeof(double) * 15 * (size_t)cap);
+        e = ctx_malloc(c, (void **)&d, sizeof(double) * 15 * (size_t)cap);
     if (e == cudaSuccess)
-        e = cudaMallocHost(&h, sizeof(double) * 15 * (size_t)cap);
+        e = ctx_malloc_host(c, (void **)&h,
+                            sizeof(double) * 15 * (size_t)cap);
     if (e != cudaSuccess) {
         if (sm)
             cudaFree(sm);
@@ -479,7 +515,7 @@ int ensure_pipeline(fvif_ctx *c)
     cudaError_t e = cudaStreamCreateWithFlags(&c->copy_stream,
                                               cudaStreamNonBlocking);
     for (int i = 0; i < c->stage_slots && e == cudaSuccess; ++i) {
-        e = cudaMalloc(&c->stage[i], slot);
+        e = ctx_malloc(c, (void **)&c->stage[i], slot);
         if (e == cudaSuccess)
             e = cudaEventCreateWithFlags(&c->copied[i],
                                          cudaEventDisableTiming);
@@ -487,7 +523,38 @@ int ensure_pipeline(fvif_ctx *c)
             e = cudaEventCreateWithFlags(&c->consumed[i],
                                          cudaEventDisableTiming);
     }
+    /* a pipeline that could not be made completely is not kept: the next
+     * call tries again instead of using missing slots */
+    if (e != cudaSuccess)
+        release_pipeline(c);
     return cuda_status(e);
+}
+
+/* FVIF_LOG set (to anything) in the environment: one line on stderr per
+ * create and score call, with its size, status and host wall time. */
+bool log_enabled()
+{
+    static const bool on = std::getenv("FVIF_LOG") != nullptr;
+    return on;
+}
+
+double ms_since(std::chrono::steady_clock::time_point t0)
+{
+    return std::chrono::duration<double, std::milli>(
+               std::chrono::steady_clock::now() - t0)
+        .count();
+}
+
+void log_call(const char *what, const fvif_ctx *c, int n_frames, int st,
+              std::chrono::steady_clock::time_point t0)
+{
+    if (!log_enabled())
+        return;
+    std::fprintf(stderr,
+                 "fvif: %s %dx%d frames=%d chunk=%d status=%d (%s) "
+                 "%.3f ms\n",
+                 what, c ? c->w : 0, c ? c->h : 0, n_frames,
+                 c ? c->chunk : 0, st, fvif_strerror(st), ms_since(t0));
 }
 
 } // namespace
@@ -511,7 +578,7 @@ fvif_ctx *fvif_create(int w, int h, int bitdepth, float kernelscale,
     return fvif_create_ex(w, h, bitdepth, kernelscale, sigma_nsq, nullptr);
 }
 
-fvif_ctx *fvif_create_ex(int w, int h, int bitdepth, float kernelscale,
+static fvif_ctx *create_ex_impl(int w, int h, int bitdepth, float kernelscale,
                          double sigma_nsq, const fvif_options *opt)
 {
     g_create_status = FVIF_EINVAL;
@@ -580,6 +647,12 @@ fvif_ctx *fvif_create_ex(int w, int h, int bitdepth, float kernelscale,
             c->chunk = v;
     }
     c->host_chunk = c->chunk < kDefaultChunk ? c->chunk : kDefaultChunk;
+    if (const char *env = std::getenv("FVIF_FAIL_ALLOC")) {
+        char *end = nullptr;
+        const long v = std::strtol(env, &end, 10);
+        if (end != env && v >= 0 && v < 1000000)
+            c->fail_alloc_at = (int)v;
+    }
     if (const char *env = std::getenv("FVIF_HOST_SLOTS")) {
         const int v = std::atoi(env);
         if (v >= 2 && v <= kMaxStage)
@@ -600,10 +673,11 @@ fvif_ctx *fvif_create_ex(int w, int h, int bitdepth, float kernelscale,
     for (int i = 0; i < kLanes && e == cudaSuccess; ++i) {
         fvif_ctx::Lane &l = c->lanes[i];
         for (int s = 1; s < kScales && e == cudaSuccess; ++s)
-            e = cudaMalloc(&l.pyr[s], sizeof(float2) * (size_t)c->ws[s] *
-                                          c->hs[s] * c->chunk);
+            e = ctx_malloc(c, (void **)&l.pyr[s],
+                           sizeof(float2) * (size_t)c->ws[s] * c->hs[s] *
+                               c->chunk);
         if (e == cudaSuccess)
-            e = cudaMalloc(&l.rows,
+            e = ctx_malloc(c, (void **)&l.rows,
                            sizeof(float2) * (size_t)rows_total * c->chunk);
         if (e == cudaSuccess)
             e = cudaStreamCreateWithFlags(&l.stream, cudaStreamNonBlocking);
@@ -613,7 +687,8 @@ fvif_ctx *fvif_create_ex(int w, int h, int bitdepth, float kernelscale,
     if (e == cudaSuccess)
         e = cudaEventCreateWithFlags(&c->fork, cudaEventDisableTiming);
     if (e == cudaSuccess)
-        e = cudaMalloc(&c->sums, sizeof(float2) * kScales * (size_t)c->chunk);
+        e = ctx_malloc(c, (void **)&c->sums,
+                       sizeof(float2) * kScales * (size_t)c->chunk);
     int st = cuda_status(e);
     if (st == FVIF_OK)
         st = ensure_out(c, c->chunk);
@@ -721,7 +796,7 @@ int fvif_get_taps(const fvif_ctx *ctx, int scale, float *taps, int cap)
     return t.n;
 }
 
-int fvif_score_async(fvif_ctx *ctx, const void *ref, const void *dist,
+static int score_async_impl(fvif_ctx *ctx, const void *ref, const void *dist,
                      int n_frames, double *out)
 {
     if (!ctx)
@@ -736,7 +811,7 @@ int fvif_score_async(fvif_ctx *ctx, const void *ref, const void *dist,
     return set_status(ctx, enqueue_all(ctx, ref, dist, n_frames, out));
 }
 
-int fvif_score(fvif_ctx *ctx, const void *ref, const void *dist, int n_frames,
+static int score_impl(fvif_ctx *ctx, const void *ref, const void *dist, int n_frames,
                double *out)
 {
     if (!ctx)
@@ -756,7 +831,7 @@ int fvif_score(fvif_ctx *ctx, const void *ref, const void *dist, int n_frames,
     return set_status(ctx, st);
 }
 
-int fvif_score_debug(fvif_ctx *ctx, const void *ref, const void *dist,
+static int score_debug_impl(fvif_ctx *ctx, const void *ref, const void *dist,
                      int n_frames, double *out)
 {
     if (!ctx)
@@ -790,7 +865,7 @@ int fvif_score_debug(fvif_ctx *ctx, const void *ref, const void *dist,
     return set_status(ctx, st);
 }
 
-int fvif_score_host(fvif_ctx *ctx, const void *ref, const void *dist,
+static int score_host_impl(fvif_ctx *ctx, const void *ref, const void *dist,
                     int n_frames, double *out)
 {
     if (!ctx)
@@ -912,7 +987,7 @@ int fvif_debug_frame(fvif_ctx *ctx, const void *ref, const void *dist,
         for (int s = 0; s < kScales; ++s)
             total += 2 * (size_t)ctx->ws[s] * ctx->hs[s];
         float *tmp = nullptr;
-        e = cudaMalloc(&tmp, sizeof(float) * total);
+        e = ctx_malloc(ctx, (void **)&tmp, sizeof(float) * total);
         size_t off = 0;
         for (int s = 0; s < kScales && e == cudaSuccess; ++s) {
             const size_t np = (size_t)ctx->ws[s] * ctx->hs[s];
@@ -948,6 +1023,57 @@ int fvif_debug_frame(fvif_ctx *ctx, const void *ref, const void *dist,
     if (e == cudaSuccess)
         e = cudaStreamSynchronize(ctx->stream);
     return set_status(ctx, cuda_status(e));
+}
+
+fvif_ctx *fvif_create_ex(int w, int h, int bitdepth, float kernelscale,
+                         double sigma_nsq, const fvif_options *opt)
+{
+    const auto t0 = std::chrono::steady_clock::now();
+    fvif_ctx *c = create_ex_impl(w, h, bitdepth, kernelscale, sigma_nsq, opt);
+    if (log_enabled())
+        std::fprintf(stderr,
+                     "fvif: create %dx%d bitdepth=%d kernelscale=%g "
+                     "sigma_nsq=%g chunk=%d status=%d (%s) %.3f ms\n",
+                     w, h, bitdepth, (double)kernelscale, sigma_nsq,
+                     c ? c->chunk : 0, fvif_last_error(c),
+                     fvif_strerror(fvif_last_error(c)), ms_since(t0));
+    return c;
+}
+
+int fvif_score(fvif_ctx *ctx, const void *ref, const void *dist, int n_frames,
+               double *out)
+{
+    const auto t0 = std::chrono::steady_clock::now();
+    const int st = score_impl(ctx, ref, dist, n_frames, out);
+    log_call("score", ctx, n_frames, st, t0);
+    return st;
+}
+
+int fvif_score_async(fvif_ctx *ctx, const void *ref, const void *dist,
+                     int n_frames, double *out)
+{
+    const auto t0 = std::chrono::steady_clock::now();
+    const int st = score_async_impl(ctx, ref, dist, n_frames, out);
+    log_call("score_async (enqueue)", ctx, n_frames, st, t0);
+    return st;
+}
+
+int fvif_score_host(fvif_ctx *ctx, const void *ref, const void *dist,
+                    int n_frames, double *out)
+{
+    const auto t0 = std::chrono::steady_clock::now();
+    const int st = score_host_impl(ctx, ref, dist, n_frames, out);
+    log_call("score_host", ctx, n_frames, st, t0);
+    return st;
+}
+
+int fvif_score_debug(fvif_ctx *ctx, const void *ref, const void *dist,
+                     int n_frames, double *out)
+{
+    const auto t0 = std::chrono::steady_clock::now();
+    const int st = score_debug_impl(ctx, ref, dist, n_frames, out);
+    log_call("score_debug", ctx, n_frames, st, t0);
+    return st;
 }
 
 } // extern "C"
