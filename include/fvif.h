@@ -29,6 +29,9 @@
  *    contents are unspecified.  The status is also kept for
  *    fvif_last_error().
  *  - A context is not thread-safe; separate contexts are independent.
+ *  - A pointer that is not a live context (destroyed, or never returned by
+ *    fvif_create) is rejected with FVIF_EINVAL and never dereferenced;
+ *    destroying it is a no-op.
  *  - All work runs on the context's CUDA stream (default: the legacy default
  *    stream; see fvif_set_stream).
  *

@@ -5,6 +5,8 @@
   FVIF_ENOMEM with nothing left behind; a failed staging allocation of
   fvif_score_host is reported, and the same context then scores correctly.
 - Canaries: sentinel values after every output buffer stay untouched.
+- A destroyed context is rejected, not dereferenced; destroying it twice is
+  a no-op.
 """
 import numpy as np
 import pytest
@@ -119,3 +121,20 @@ def test_decimation_writes_only_its_outputs(fv, w, h, bitdepth, scale):
         host = b.cpu().numpy()
         assert np.all(host[n:] == -7.5)
         assert np.array_equal(host[:n].view(np.uint32), o.ravel().view(np.uint32))
+
+
+def test_use_after_destroy_is_rejected(fv):
+    import torch
+    L = fv.lib()
+    ctx = L.fvif_create(96, 64, 10, 1.0, 2.0)
+    assert ctx and L.fvif_chunk_frames(ctx) > 0
+    L.fvif_destroy(ctx)
+    r = torch.zeros(96 * 64, dtype=torch.int16, device="cuda")
+    out = np.zeros(4, np.float64)
+    assert L.fvif_score(ctx, r.data_ptr(), r.data_ptr(), 1,
+                        out.ctypes.data) == fv.FVIF_EINVAL
+    assert L.fvif_chunk_frames(ctx) == fv.FVIF_EINVAL
+    L.fvif_destroy(ctx)              # a second destroy is a no-op
+    ctx2 = L.fvif_create(96, 64, 10, 1.0, 2.0)
+    assert ctx2
+    L.fvif_destroy(ctx2)

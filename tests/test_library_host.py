@@ -196,3 +196,22 @@ def test_fvif_log_lines_for_rejected_calls(L):
                        env={k: v for k, v in env.items() if k != "FVIF_LOG"},
                        capture_output=True, text=True, timeout=120)
     assert r.returncode == 0 and "fvif: " not in r.stderr
+
+
+def test_stray_context_pointers_are_rejected(L):
+    """A pointer that is not a live context is rejected with FVIF_EINVAL by
+    every entry point, never dereferenced (no GPU needed)."""
+    bogus = ctypes.c_void_p(0x1000)
+    buf = ctypes.c_void_p(0x2000)
+    E = fv.FVIF_EINVAL
+    assert L.fvif_score(bogus, buf, buf, 1, buf) == E
+    assert L.fvif_score_async(bogus, buf, buf, 1, buf) == E
+    assert L.fvif_score_host(bogus, buf, buf, 1, buf) == E
+    assert L.fvif_score_debug(bogus, buf, buf, 1, buf) == E
+    assert L.fvif_set_stream(bogus, None) == E
+    assert L.fvif_chunk_frames(bogus) == E
+    assert L.fvif_last_error(bogus) == E
+    taps = (ctypes.c_float * 64)()
+    assert L.fvif_get_taps(bogus, 0, taps, 64) == E
+    L.fvif_destroy(bogus)            # a no-op
+    L.fvif_destroy(None)

@@ -8,7 +8,9 @@
 #include <vector>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <new>
+#include <unordered_set>
 
 #include "../../include/fvif.h"
 #include "fvif_internal.h"
@@ -24,6 +26,20 @@ constexpr int kLanes = 2; /* chunks alternate between two streams */
 constexpr int kMaxStage = 4; /* host-input staging slots, at most */
 
 thread_local int g_create_status = FVIF_OK;
+
+/* Contexts made by fvif_create and not yet destroyed: every entry point
+ * rejects any other pointer (a destroyed context, a stray value) with
+ * FVIF_EINVAL instead of dereferencing it. */
+std::mutex g_live_mutex;
+std::unordered_set<const fvif_ctx *> g_live;
+
+bool live(const fvif_ctx *c)
+{
+    if (!c)
+        return false;
+    std::lock_guard<std::mutex> lock(g_live_mutex);
+    return g_live.count(c) != 0;
+}
 
 } // namespace
 
@@ -550,6 +566,8 @@ void log_call(const char *what, const fvif_ctx *c, int n_frames, int st,
 {
     if (!log_enabled())
         return;
+    if (!live(c))
+        c = nullptr;     /* a stray pointer is reported, not read */
     std::fprintf(stderr,
                  "fvif: %s %dx%d frames=%d chunk=%d status=%d (%s) "
                  "%.3f ms\n",
@@ -704,8 +722,11 @@ static fvif_ctx *create_ex_impl(int w, int h, int bitdepth, float kernelscale,
 
 void fvif_destroy(fvif_ctx *ctx)
 {
-    if (!ctx)
-        return;
+    {
+        std::lock_guard<std::mutex> lock(g_live_mutex);
+        if (!ctx || g_live.erase(ctx) == 0)
+            return;
+    }
     DeviceGuard g(ctx->device);
     cudaStreamSynchronize(ctx->stream);
     for (fvif_ctx::Lane &l : ctx->lanes)
@@ -717,7 +738,7 @@ void fvif_destroy(fvif_ctx *ctx)
 
 int fvif_set_stream(fvif_ctx *ctx, void *cuda_stream)
 {
-    if (!ctx)
+    if (!live(ctx))
         return FVIF_EINVAL;
     ctx->stream = static_cast<cudaStream_t>(cuda_stream);
     return set_status(ctx, FVIF_OK);
@@ -725,7 +746,9 @@ int fvif_set_stream(fvif_ctx *ctx, void *cuda_stream)
 
 int fvif_last_error(const fvif_ctx *ctx)
 {
-    return ctx ? ctx->last_status : g_create_status;
+    if (!ctx)
+        return g_create_status;
+    return live(ctx) ? ctx->last_status : FVIF_EINVAL;
 }
 
 const char *fvif_strerror(int status)
@@ -743,7 +766,7 @@ const char *fvif_strerror(int status)
 
 int fvif_profile_enable(fvif_ctx *ctx, int enable)
 {
-    if (!ctx)
+    if (!live(ctx))
         return FVIF_EINVAL;
     DeviceGuard g(ctx->device);
     if (cudaStreamSynchronize(ctx->stream) != cudaSuccess)
@@ -782,12 +805,12 @@ int fvif_profile_read(fvif_ctx *ctx, int kind, double *total_ms,
 
 int fvif_chunk_frames(const fvif_ctx *ctx)
 {
-    return ctx ? ctx->chunk : FVIF_EINVAL;
+    return live(ctx) ? ctx->chunk : FVIF_EINVAL;
 }
 
 int fvif_get_taps(const fvif_ctx *ctx, int scale, float *taps, int cap)
 {
-    if (!ctx || !taps || scale < 0 || scale >= kScales)
+    if (!live(ctx) || !taps || scale < 0 || scale >= kScales)
         return FVIF_EINVAL;
     const Taps &t = ctx->taps[scale];
     if (cap < t.n)
@@ -799,7 +822,7 @@ int fvif_get_taps(const fvif_ctx *ctx, int scale, float *taps, int cap)
 static int score_async_impl(fvif_ctx *ctx, const void *ref, const void *dist,
                      int n_frames, double *out)
 {
-    if (!ctx)
+    if (!live(ctx))
         return FVIF_EINVAL;
     if (n_frames < 0 || (n_frames > 0 && (!ref || !dist || !out)))
         return set_status(ctx, FVIF_EINVAL);
@@ -814,7 +837,7 @@ static int score_async_impl(fvif_ctx *ctx, const void *ref, const void *dist,
 static int score_impl(fvif_ctx *ctx, const void *ref, const void *dist, int n_frames,
                double *out)
 {
-    if (!ctx)
+    if (!live(ctx))
         return FVIF_EINVAL;
     if (n_frames < 0 || (n_frames > 0 && (!ref || !dist || !out)))
         return set_status(ctx, FVIF_EINVAL);
@@ -834,7 +857,7 @@ static int score_impl(fvif_ctx *ctx, const void *ref, const void *dist, int n_fr
 static int score_debug_impl(fvif_ctx *ctx, const void *ref, const void *dist,
                      int n_frames, double *out)
 {
-    if (!ctx)
+    if (!live(ctx))
         return FVIF_EINVAL;
     if (n_frames < 0 || (n_frames > 0 && (!ref || !dist || !out)))
         return set_status(ctx, FVIF_EINVAL);
@@ -868,7 +891,7 @@ static int score_debug_impl(fvif_ctx *ctx, const void *ref, const void *dist,
 static int score_host_impl(fvif_ctx *ctx, const void *ref, const void *dist,
                     int n_frames, double *out)
 {
-    if (!ctx)
+    if (!live(ctx))
         return FVIF_EINVAL;
     if (n_frames < 0 || (n_frames > 0 && (!ref || !dist || !out)))
         return set_status(ctx, FVIF_EINVAL);
@@ -946,7 +969,7 @@ int fvif_debug_terms(fvif_ctx *ctx, const float *mu1, const float *mu2,
                      int n, float *num, float *den,
                      unsigned long long *fallbacks)
 {
-    if (!ctx)
+    if (!live(ctx))
         return FVIF_EINVAL;
     if (n < 0 || (n > 0 && (!mu1 || !mu2 || !xx || !yy || !xy || !num ||
                             !den)))
@@ -964,7 +987,7 @@ int fvif_debug_terms(fvif_ctx *ctx, const float *mu1, const float *mu2,
 int fvif_debug_frame(fvif_ctx *ctx, const void *ref, const void *dist,
                      float *planes, float *rows, float *sums)
 {
-    if (!ctx)
+    if (!live(ctx))
         return FVIF_EINVAL;
     if (!ref || !dist)
         return set_status(ctx, FVIF_EINVAL);
@@ -1030,6 +1053,10 @@ fvif_ctx *fvif_create_ex(int w, int h, int bitdepth, float kernelscale,
 {
     const auto t0 = std::chrono::steady_clock::now();
     fvif_ctx *c = create_ex_impl(w, h, bitdepth, kernelscale, sigma_nsq, opt);
+    if (c) {
+        std::lock_guard<std::mutex> lock(g_live_mutex);
+        g_live.insert(c);
+    }
     if (log_enabled())
         std::fprintf(stderr,
                      "fvif: create %dx%d bitdepth=%d kernelscale=%g "
