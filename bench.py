@@ -63,7 +63,7 @@ def describe(name, frames_override=None):
     case_name, frames, ks = WORKLOADS[name]
     frames = frames_override or frames
     c = S.CASES[case_name]
-    return ("%s: %dx%d %d-bit luma pairs, %d frames per step in chunks of 16, "
+    return ("%s: %dx%d %d-bit luma pairs, %d frames per step, "
             "kernelscale %g, sigma_nsq %g" % (case_name, c.w, c.h, c.bitdepth,
                                               frames, ks, c.nsq))
 
