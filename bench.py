@@ -499,7 +499,7 @@ def run_ours(args):
             "solo_achieved": ops_solo / (solo_ms / 1e3) / 1e12,
             "solo_frac": ops_solo / (solo_ms / 1e3) / 1e12 / alu_peak,
             "solo_note": "the same launch with no other chunk in flight "
-                         "(one 16-frame chunk scored alone after the timed "
+                         "(one chunk scored alone after the timed "
                          "region, events on its stream)",
             "step_achieved": step_ops / (ms_step / 1e3) / 1e12,
             "step_frac": step_ops / (ms_step / 1e3) / 1e12 / alu_peak,
