@@ -300,3 +300,31 @@ def test_planar_yuv_frames(fv, factor, bd):
         assert_bitwise(ctx.score_host(rbuf, dbuf), want, "host %s" % factor)
         assert_bitwise(ctx.score_debug(to_device(rbuf), to_device(dbuf))[:, :4],
                        want, "debug %s" % factor)
+
+
+@pytest.mark.parametrize("w,h,bitdepth", [
+    (16384, 48, 10), (48, 16384, 10), (16384, 4096, 8),
+])
+def test_largest_frame_sides(fv, w, h, bitdepth):
+    """The largest side the library accepts (16384 samples), in full against
+    the oracle: one frame pair each (16384 x 4096 is 67 M pixels)."""
+    case = S.custom_noise_case(w, h, bitdepth, frames=1, seed=5)
+    ref, dist = case.batch(range(1))
+    for ks in (1.0,):
+        got = gpu_scores(fv, case, ref, dist, ks, 2.0)
+        want = oracle_scores(ref, dist, bitdepth, ks, 2.0)
+        assert_bitwise(got, want, "%dx%d %d-bit" % (w, h, bitdepth))
+
+
+def test_largest_frame_black_pair_scores_exactly_one(fv):
+    """16384 x 16384 (268 M pixels per plane), the largest frame accepted:
+    black frames give exactly 0 for every filtered quantity, so every pixel
+    of every scale takes the low-variance branch with sigma2_sq = 0 and every
+    scale scores exactly 1.0 (the oracle's pin on black frames).  Real
+    content at the largest side is checked in full at 16384 x 4096."""
+    torch = torch_mod()
+    w = h = 16384
+    with fv.Context(w, h, 8, 1.0, 2.0) as ctx:
+        r = torch.zeros((1, h, w), dtype=torch.uint8, device="cuda")
+        got = ctx.score(r, r.clone())
+    assert np.array_equal(got, np.ones((1, 4))), got
