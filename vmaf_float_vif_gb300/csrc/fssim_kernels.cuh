@@ -24,20 +24,30 @@
  * applied exactly.  For power-of-two k the tap is exact: e = 0 and the output
  * is fl(sum(s)) * t * 2^-q.
  *
- * Work split: a block takes R output rows by X output columns of one plane of
- * one frame.  Phase 1: each thread sums V adjacent input columns (one 16-byte
- * load per row on the vector path) over the k window rows of its output
- * rows, into sum(s) as integers and sum(e) as fp32.  The fp32 sum is exact:
- * each partial sum is a multiple of 2^-E below k * 2^15 * 2^-E < 2^24 * 2^-E.
- * The loads of a batch of rows are all issued before any is added.  The
- * column sums go to shared memory as integers.  Phase 2: each thread adds the
- * k columns of one output window, mirrored at the edges, and rounds once.
+ * Three kernels, chosen per sample type and scale (measured at 4K):
+ *  - ssim_decimate_u8_partials_kernel: 8-bit samples, k = 4 or 8, 16-byte
+ *    rows: window partial sums with dp4a, no shared memory; at the HBM
+ *    bound.
+ *  - ssim_decimate_windows_kernel: k = 2..8, 16-byte rows: each thread owns
+ *    16 (8-bit) or 8 (16-bit) whole windows.
+ *  - ssim_decimate_kernel, the general two-phase kernel, for every other
+ *    case (any scale, any alignment).  A block takes R output rows by X
+ *    output columns of one plane of one frame.  Phase 1: each thread sums V
+ *    adjacent input columns (one 16-byte load per row on the vector path)
+ *    over the k window rows of its output rows, into sum(s) as integers and
+ *    sum(e) as fp32.  The fp32 sum is exact: each partial sum is a multiple
+ *    of 2^-E below k * 2^15 * 2^-E < 2^24 * 2^-E.  The loads of a batch of
+ *    rows are all issued before any is added.  The column sums go to shared
+ *    memory as integers.  Phase 2: each thread adds the k columns of one
+ *    output window, mirrored at the edges, and rounds once.
  * Every input byte is read from DRAM once (edge windows re-read mirrored
- * columns from shared memory), so the kernel is bound by HBM bandwidth.
+ * columns from shared memory or neighbouring lanes).  Exact taps are bound
+ * by HBM bandwidth; inexact taps add about four instructions per sample for
+ * the product error and are bound by instruction issue at 8 bits.
  *
  * The scales 2..8 (the auto scales of frames up to 8.5K wide) are compiled
- * with k fixed, so the row and column loops unroll; other scales run the same
- * kernel with k read at run time.
+ * with k fixed, so the row and column loops unroll; other scales run the
+ * general kernel with k read at run time.
  */
 #ifndef FSSIM_KERNELS_CUH
 #define FSSIM_KERNELS_CUH
@@ -55,7 +65,6 @@ constexpr int kMaxRows = 16;                // output rows per block
 constexpr size_t kMaxSmem = 64 * 1024;      // shared bytes per block
 constexpr int kMaxFramesPerLaunch = 32767;  // grid.z = 2 * frames
 constexpr int kBatch = 8;                   // rows loaded before any is added
-constexpr int kMaxFixedScale = 8;           // scales compiled with k fixed
 
 struct DecimateParams {
     const void *src[2];       // ref, dist
