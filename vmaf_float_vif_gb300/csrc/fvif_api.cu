@@ -165,9 +165,15 @@ struct fvif_ctx {
     struct Lane {
         float2 *pyr[kScales] = {}; /* scales 1..3, chunk frames each      */
         float2 *rows = nullptr;    /* chunk frames x sum(h_s) (num, den)  */
-        cudaStream_t stream = nullptr;
+        cudaStream_t stream = nullptr; /* low priority                     */
         cudaEvent_t done = nullptr;
+        cudaEvent_t free_ev = nullptr; /* lane work before this chunk done */
+        cudaEvent_t s0_done = nullptr; /* this chunk's scale-0 statistic   */
     } lanes[kLanes];
+    /* Every scale-0 statistic launch runs on this one high-priority stream,
+     * one chunk after the other: each gets the GPU to itself, and the
+     * lanes' smaller kernels (low priority) fill the SMs it leaves idle. */
+    cudaStream_t big = nullptr;
     cudaEvent_t fork = nullptr;
     int rows_stride = 0;
     int rows_base[kScales] = {};
@@ -267,7 +273,13 @@ void release(fvif_ctx *c)
             cudaStreamDestroy(l.stream);
         if (l.done)
             cudaEventDestroy(l.done);
+        if (l.free_ev)
+            cudaEventDestroy(l.free_ev);
+        if (l.s0_done)
+            cudaEventDestroy(l.s0_done);
     }
+    if (c->big)
+        cudaStreamDestroy(c->big);
     if (c->fork)
         cudaEventDestroy(c->fork);
     if (c->sums)
@@ -349,7 +361,12 @@ int run_chunk(fvif_ctx *c, fvif_ctx::Lane &l, const void *ref,
 {
     cudaStream_t st = l.stream;
     const SrcDesc s0 = scale0_src(c, ref, dist, in_frame_elems);
-    cudaError_t e = cudaSuccess;
+    /* the scale-0 statistic of this chunk may start once everything queued
+     * on the lane before it is done (its input copied, the chunk that used
+     * the lane's buffers before it reduced) */
+    cudaError_t e = cudaEventRecord(l.free_ev, st);
+    if (e == cudaSuccess)
+        e = cudaStreamWaitEvent(c->big, l.free_ev, 0);
 
     for (int s = 1; s < kScales && e == cudaSuccess; ++s) {
         DecArgs d;
@@ -378,12 +395,18 @@ int run_chunk(fvif_ctx *c, fvif_ctx::Lane &l, const void *ref,
         a.rows_stride = c->rows_stride;
         a.rows_base = c->rows_base[s];
         const int kind = s == 0 ? FVIF_K_STATS0 : FVIF_K_STATS123;
-        e = prof_begin(c, kind, st);
+        cudaStream_t ks = s == 0 ? c->big : st;
+        e = prof_begin(c, kind, ks);
         if (e == cudaSuccess)
-            e = launch_stats(a, c->taps[s], st);
+            e = launch_stats(a, c->taps[s], ks);
         if (e == cudaSuccess)
-            e = prof_end(c, kind, st);
+            e = prof_end(c, kind, ks);
+        if (e == cudaSuccess && s == 0)
+            e = cudaEventRecord(l.s0_done, c->big);
     }
+    /* the reduction reads the scale-0 row sums */
+    if (e == cudaSuccess && !c->skip_scale0)
+        e = cudaStreamWaitEvent(st, l.s0_done, 0);
     if (e == cudaSuccess) {
         FinalArgs f;
         f.rows = l.rows;
@@ -413,6 +436,8 @@ cudaError_t fork_lanes(fvif_ctx *c)
     cudaError_t e = cudaEventRecord(c->fork, c->stream);
     for (int i = 0; i < kLanes && e == cudaSuccess; ++i)
         e = cudaStreamWaitEvent(c->lanes[i].stream, c->fork, 0);
+    if (e == cudaSuccess)
+        e = cudaStreamWaitEvent(c->big, c->fork, 0);
     return e;
 }
 
@@ -682,6 +707,9 @@ static fvif_ctx *create_ex_impl(int w, int h, int bitdepth, float kernelscale,
             c->host_lanes = v;
     }
     cudaError_t e = cudaGetDevice(&c->device);
+    int prio_low = 0, prio_high = 0;
+    if (e == cudaSuccess)
+        e = cudaDeviceGetStreamPriorityRange(&prio_low, &prio_high);
     int rows_total = 0;
     for (int s = 0; s < kScales; ++s) {
         c->rows_base[s] = rows_total;
@@ -698,10 +726,18 @@ static fvif_ctx *create_ex_impl(int w, int h, int bitdepth, float kernelscale,
             e = ctx_malloc(c, (void **)&l.rows,
                            sizeof(float2) * (size_t)rows_total * c->chunk);
         if (e == cudaSuccess)
-            e = cudaStreamCreateWithFlags(&l.stream, cudaStreamNonBlocking);
+            e = cudaStreamCreateWithPriority(&l.stream, cudaStreamNonBlocking,
+                                             prio_low);
         if (e == cudaSuccess)
             e = cudaEventCreateWithFlags(&l.done, cudaEventDisableTiming);
+        if (e == cudaSuccess)
+            e = cudaEventCreateWithFlags(&l.free_ev, cudaEventDisableTiming);
+        if (e == cudaSuccess)
+            e = cudaEventCreateWithFlags(&l.s0_done, cudaEventDisableTiming);
     }
+    if (e == cudaSuccess)
+        e = cudaStreamCreateWithPriority(&c->big, cudaStreamNonBlocking,
+                                         prio_high);
     if (e == cudaSuccess)
         e = cudaEventCreateWithFlags(&c->fork, cudaEventDisableTiming);
     if (e == cudaSuccess)
