@@ -110,13 +110,32 @@ def test_edge_sizes(fv, w, h):
         assert_bitwise(got, want, "%dx%d ks=%g" % (w, h, ks))
 
 
-@pytest.mark.parametrize("bd", [9, 10, 12, 16])
-def test_bit_depths(fv, bd):
+@pytest.mark.parametrize("bd", [9, 10, 12, 14, 16])
+@pytest.mark.parametrize("ks", [0.5, 1.0, 2.0])
+def test_bit_depths(fv, bd, ks):
+    """Every fixed-width kernel that reads 16-bit samples (they multiply the
+    unscaled samples by prescaled taps)."""
     case = S.custom_noise_case(180, 100, bd, frames=2)
     ref, dist = case.batch(range(2))
-    got = gpu_scores(fv, case, ref, dist, 1.0, 2.0)
+    got = gpu_scores(fv, case, ref, dist, ks, 2.0)
+    want = oracle_scores(ref, dist, bd, ks, 2.0)
+    assert_bitwise(got, want, "bitdepth %d ks=%g" % (bd, ks))
+
+
+@pytest.mark.parametrize("bd", [10, 16])
+def test_full_range_samples(fv, bd):
+    """Samples at 0 and at the top code of the bit depth, next to each
+    other: the largest squares the 16-bit path forms."""
+    rng = np.random.default_rng(bd)
+    top = (1 << bd) - 1
+    shape = (2, 72, 120)
+    ref = (rng.integers(0, 2, shape) * top).astype(np.uint16)
+    dist = np.clip(ref.astype(np.int64) - rng.integers(0, 3, shape), 0,
+                   top).astype(np.uint16)
     want = oracle_scores(ref, dist, bd, 1.0, 2.0)
-    assert_bitwise(got, want, "bitdepth %d" % bd)
+    with fv.Context(120, 72, bd, 1.0, 2.0) as ctx:
+        assert_bitwise(ctx.score(to_device(ref), to_device(dist)), want,
+                       "%d-bit extremes" % bd)
 
 
 @pytest.mark.parametrize("ks", [0.25, 0.75, 1.5, 3.0, 7.5])

@@ -2,6 +2,7 @@
  * fvif_api.cu -- host side of libfvif: context, taps, chunked launches and
  * the C ABI declared in include/fvif.h.
  */
+#include <cfloat>
 #include <cmath>
 #include <chrono>
 #include <cstdio>
@@ -81,7 +82,23 @@ int make_taps(float kernelscale, int s, Taps &out)
         out.t[k] = (float)(wk[k] / sum);
     for (int k = 0; k < out.n; ++k)
         out.t2[k] = make_float2(out.t[k], out.t[k]);
+    set_sample_taps(out, 8);
     return FVIF_OK;
+}
+
+void set_sample_taps(Taps &t, int bitdepth)
+{
+    const int q = bitdepth > 8 ? bitdepth - 8 : 0;
+    t.raw_ok = t.n <= kMaxFixedTaps;
+    for (int k = 0; k < kMaxFixedTaps; ++k) {
+        const float a = k < t.n ? std::ldexp(t.t[k], -q) : 0.0f;
+        const float b = k < t.n ? std::ldexp(t.t[k], -2 * q) : 0.0f;
+        if (k < t.n && (!(std::fabs(a) >= FLT_MIN) || !(std::fabs(b) >= FLT_MIN)))
+            t.raw_ok = 0;
+        t.ra2[k] = make_float2(a, a);
+        t.rb2[k] = make_float2(b, b);
+        t.rc[k] = b;
+    }
 }
 
 /* Constants of the per-pixel statistic.  nsq_up makes the fp64 comparison
@@ -674,6 +691,7 @@ static fvif_ctx *create_ex_impl(int w, int h, int bitdepth, float kernelscale,
             delete c;
             return nullptr;
         }
+        set_sample_taps(c->taps[s], bitdepth);
     }
     /* Frames per chunk: enough that the scale-0 statistic launch has about
      * kChunkCtas CTAs (one per 16-row strip and frame; measured best for

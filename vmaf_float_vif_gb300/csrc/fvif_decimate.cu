@@ -44,7 +44,8 @@ template <SrcKind K>
 static cudaError_t dec_dispatch_u(const DecArgs &a, const Taps &tp,
                                   cudaStream_t st)
 {
-    switch (tp.n) {
+    /* 16-bit fixed widths read the samples against prescaled taps */
+    switch (K == SrcKind::U16 && !tp.raw_ok ? 0 : tp.n) {
     case 5: return run_decimate<5, K>(a, tp, st);
     case 9: return run_decimate<9, K>(a, tp, st);
     case 19: return run_decimate<19, K>(a, tp, st);

@@ -16,12 +16,27 @@ constexpr int kMaxTaps = 2 * kMaxRadius + 1; /* 129                          */
 
 /* Taps of one scale, handed to a launch by value (kernel parameter space),
  * so compile-time-indexed reads become constant-bank operands.            */
+constexpr int kMaxFixedTaps = 35; /* widest kernel compiled with fixed N */
+
 struct Taps {
     float t[kMaxTaps];
     float2 t2[kMaxTaps]; /* (t[k], t[k]) for the packed two-lane operations */
+    /* Vertical-pass taps for 16-bit integer samples s = x * 2^q (fixed
+     * widths): t * x and t * (s * 2^-q) are the same real product, so
+     * fl(t * x) = fl((t * 2^-q) * s); likewise fl(t * fl(x * x)) =
+     * fl((t * 2^-2q) * fl(s * s)) and the same for x * y.  The scale-0
+     * passes read the samples without rescaling them.  raw_ok is set when
+     * every prescaled tap is a normal fp32 value (the identity needs it). */
+    float2 ra2[kMaxFixedTaps]; /* (t 2^-q, t 2^-q)     for (x, y)           */
+    float2 rb2[kMaxFixedTaps]; /* (t 2^-2q, t 2^-2q)   for (x*x, y*y)       */
+    float rc[kMaxFixedTaps];   /* t 2^-2q              for x*y              */
+    int raw_ok;
     float2 one2;         /* (1, 1), read at run time (see acc2_rn)          */
     int n;
 };
+
+/* Fill ra2 / rb2 / rc / raw_ok of taps for samples of this bit depth. */
+void set_sample_taps(Taps &t, int bitdepth);
 
 /* Where the samples of one plane come from. */
 enum class SrcKind { U8, U16, F2 };

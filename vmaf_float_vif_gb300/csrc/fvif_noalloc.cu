@@ -90,6 +90,7 @@ extern "C" int fvif_score_noalloc(int w, int h, int bitdepth,
         hs[s] = s == 0 ? h : hs[s - 1] / 2;
         if (make_taps(kernelscale, s, taps[s]) != FVIF_OK)
             return FVIF_EINVAL;
+        set_sample_taps(taps[s], bitdepth);
     }
 
     /* layout of the scratch for one frame */
