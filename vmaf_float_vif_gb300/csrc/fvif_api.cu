@@ -89,12 +89,15 @@ int make_taps(float kernelscale, int s, Taps &out)
 void set_sample_taps(Taps &t, int bitdepth)
 {
     const int q = bitdepth > 8 ? bitdepth - 8 : 0;
-    t.raw_ok = t.n <= kMaxFixedTaps;
+    t.fixed_ok = t.n <= kMaxFixedTaps;
+    for (int k = 0; k < t.n; ++k)
+        if (t.t[k] != t.t[t.n - 1 - k])
+            t.fixed_ok = 0;
     for (int k = 0; k < kMaxFixedTaps; ++k) {
         const float a = k < t.n ? std::ldexp(t.t[k], -q) : 0.0f;
         const float b = k < t.n ? std::ldexp(t.t[k], -2 * q) : 0.0f;
         if (k < t.n && (!(std::fabs(a) >= FLT_MIN) || !(std::fabs(b) >= FLT_MIN)))
-            t.raw_ok = 0;
+            t.fixed_ok = 0;
         t.ra2[k] = make_float2(a, a);
         t.rb2[k] = make_float2(b, b);
         t.rc[k] = b;

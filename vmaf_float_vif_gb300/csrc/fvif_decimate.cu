@@ -8,29 +8,6 @@ cudaError_t stats_dispatch_u8(const StatsArgs &, const Taps &, cudaStream_t);
 cudaError_t stats_dispatch_u16(const StatsArgs &, const Taps &, cudaStream_t);
 cudaError_t stats_dispatch_f2(const StatsArgs &, const Taps &, cudaStream_t);
 
-static const int kSpecU[] = {5, 9, 19};
-static const int kSpecF2[] = {1, 3, 5, 7, 11};
-static const int kSpecStats[] = {1, 3, 5, 7, 9, 11, 17, 19, 35};
-
-bool stats_is_specialised(int ntaps)
-{
-    for (int n : kSpecStats)
-        if (n == ntaps)
-            return true;
-    return false;
-}
-
-bool decimate_is_specialised(int ntaps)
-{
-    for (int n : kSpecU)
-        if (n == ntaps)
-            return true;
-    for (int n : kSpecF2)
-        if (n == ntaps)
-            return true;
-    return false;
-}
-
 cudaError_t launch_stats(const StatsArgs &a, const Taps &tp, cudaStream_t st)
 {
     switch (a.src.kind) {
@@ -44,8 +21,7 @@ template <SrcKind K>
 static cudaError_t dec_dispatch_u(const DecArgs &a, const Taps &tp,
                                   cudaStream_t st)
 {
-    /* 16-bit fixed widths read the samples against prescaled taps */
-    switch (K == SrcKind::U16 && !tp.raw_ok ? 0 : tp.n) {
+    switch (tp.fixed_ok ? tp.n : 0) {
     case 5: return run_decimate<5, K>(a, tp, st);
     case 9: return run_decimate<9, K>(a, tp, st);
     case 19: return run_decimate<19, K>(a, tp, st);
@@ -59,7 +35,7 @@ cudaError_t launch_decimate(const DecArgs &a, const Taps &tp, cudaStream_t st)
     case SrcKind::U8: return dec_dispatch_u<SrcKind::U8>(a, tp, st);
     case SrcKind::U16: return dec_dispatch_u<SrcKind::U16>(a, tp, st);
     default:
-        switch (tp.n) {
+        switch (tp.fixed_ok ? tp.n : 0) {
         case 1: return run_decimate<1, SrcKind::F2>(a, tp, st);
         case 3: return run_decimate<3, SrcKind::F2>(a, tp, st);
         case 5: return run_decimate<5, SrcKind::F2>(a, tp, st);

@@ -25,17 +25,20 @@ struct Taps {
      * widths): t * x and t * (s * 2^-q) are the same real product, so
      * fl(t * x) = fl((t * 2^-q) * s); likewise fl(t * fl(x * x)) =
      * fl((t * 2^-2q) * fl(s * s)) and the same for x * y.  The scale-0
-     * passes read the samples without rescaling them.  raw_ok is set when
-     * every prescaled tap is a normal fp32 value (the identity needs it). */
+     * passes read the samples without rescaling them.                      */
     float2 ra2[kMaxFixedTaps]; /* (t 2^-q, t 2^-q)     for (x, y)           */
     float2 rb2[kMaxFixedTaps]; /* (t 2^-2q, t 2^-2q)   for (x*x, y*y)       */
     float rc[kMaxFixedTaps];   /* t 2^-2q              for x*y              */
-    int raw_ok;
+    /* The fixed-width kernels may be used: n <= kMaxFixedTaps, the taps
+     * are exactly symmetric (t[k] == t[n-1-k]: those kernels form each
+     * product of a sample with a tap pair once) and every prescaled tap is
+     * a normal fp32 value (the identity above needs it).                  */
+    int fixed_ok;
     float2 one2;         /* (1, 1), read at run time (see acc2_rn)          */
     int n;
 };
 
-/* Fill ra2 / rb2 / rc / raw_ok of taps for samples of this bit depth. */
+/* Fill ra2 / rb2 / rc / fixed_ok of taps for samples of this bit depth. */
 void set_sample_taps(Taps &t, int bitdepth);
 
 /* Where the samples of one plane come from. */
@@ -125,9 +128,5 @@ cudaError_t launch_debug(const double *scores, const float2 *sums, int n,
 cudaError_t launch_unpack_planes(const SrcDesc &src, int w, int h,
                                  float *ref_out, float *dist_out,
                                  cudaStream_t st);
-
-/* Tap widths that have a specialised (fully unrolled) kernel. */
-bool stats_is_specialised(int ntaps);
-bool decimate_is_specialised(int ntaps);
 
 } // namespace fvif

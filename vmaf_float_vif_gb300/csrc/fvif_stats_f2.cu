@@ -8,7 +8,7 @@ namespace fvif {
 cudaError_t stats_dispatch_f2(const StatsArgs &a, const Taps &tp,
                               cudaStream_t st)
 {
-    switch (tp.n) {
+    switch (tp.fixed_ok ? tp.n : 0) {
     case 1: return run_stats<1, SrcKind::F2>(a, tp, st);
     case 3: return run_stats<3, SrcKind::F2>(a, tp, st);
     case 5: return run_stats<5, SrcKind::F2>(a, tp, st);

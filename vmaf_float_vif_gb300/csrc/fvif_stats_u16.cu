@@ -8,8 +8,7 @@ namespace fvif {
 cudaError_t stats_dispatch_u16(const StatsArgs &a, const Taps &tp,
                                 cudaStream_t st)
 {
-    /* the fixed widths read the samples against prescaled taps */
-    switch (tp.raw_ok ? tp.n : 0) {
+    switch (tp.fixed_ok ? tp.n : 0) {
     case 9: return run_stats<9, SrcKind::U16>(a, tp, st);
     case 17: return run_stats<17, SrcKind::U16>(a, tp, st);
     case 35: return run_stats<35, SrcKind::U16>(a, tp, st);

@@ -8,7 +8,7 @@ namespace fvif {
 cudaError_t stats_dispatch_u8(const StatsArgs &a, const Taps &tp,
                                 cudaStream_t st)
 {
-    switch (tp.n) {
+    switch (tp.fixed_ok ? tp.n : 0) {
     case 9: return run_stats<9, SrcKind::U8>(a, tp, st);
     case 17: return run_stats<17, SrcKind::U8>(a, tp, st);
     case 35: return run_stats<35, SrcKind::U8>(a, tp, st);
