@@ -28,12 +28,12 @@ __global__ void packed_check_kernel(const float *a, const float *b,
     }
     /* form 1: mac5 chain with register operands, form 2: taps from memory */
     fvif::Acc5 m5;
-    fvif::mac5(m5, true, A, A.x, B, B, B.x, one);
+    fvif::mac5(m5, true, A, A, A.x, B, B, B.x, one);
     float ax = __fmul_rn(A.x, B.x), ay = __fmul_rn(A.y, B.y);
     for (int k = 1; k < 8; ++k) {
         const float2 q = make_float2(a[(i + k) % n], c[(i + 3 * k) % n]);
         const float2 t = form == 2 ? c_taps[k] : A;
-        fvif::mac5(m5, false, t, t.x, q, q, q.x, one);
+        fvif::mac5(m5, false, t, t, t.x, q, q, q.x, one);
         ax = __fadd_rn(ax, __fmul_rn(t.x, q.x));
         ay = __fadd_rn(ay, __fmul_rn(t.y, q.y));
     }
