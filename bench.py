@@ -474,6 +474,13 @@ def run_ours(args):
             "hbm_fraction_note": "input bytes only (%d B per pair) against "
                                  "%.1f GB/s %s" % (bpp, hbm_peak, hbm_src),
             "kernels": kernel_shares,
+            "kernels_note": "summed event durations of each kind's launches "
+                            "on their own streams over the timed steps; the "
+                            "scale-0 stream and the two lanes overlap, and a "
+                            "low-priority launch's duration includes the time "
+                            "it waits for SMs, so these overlap and exceed "
+                            "the step (serialised shares: the ncu launch "
+                            "list under profiles/)",
         },
         "roofline": {
             "kernel": "stats_kernel, scale 0 (%d taps), %.4g frames per "
