@@ -26,6 +26,7 @@ import gc
 import hashlib
 import json
 import os
+import re
 import subprocess
 import sys
 import threading
@@ -196,13 +197,22 @@ def host_cores():
 # ---------------------------------------------------------------------------
 
 
-def kernel_hash():
+def source_hash(names):
+    """Hash of the named CUDA sources with comments and whitespace removed:
+    it changes with the code the counters were taken on, not with its
+    comments."""
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, "vmaf_float_vif_gb300", "csrc", f),
-                  "rb") as fh:
-            h.update(fh.read())
+    for n in names:
+        with open(os.path.join(ROOT, "vmaf_float_vif_gb300", "csrc", n)) as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
+
+
+def kernel_hash():
+    return source_hash(KERNEL_SOURCES)
 
 
 def load_traffic(workload, frames_per_launch):
@@ -551,12 +561,7 @@ SSIM_KERNEL_SOURCES = ["fssim_kernels.cuh", "fssim_u8.cu", "fssim_u16.cu",
 
 
 def ssim_kernel_hash():
-    h = hashlib.sha256()
-    for n in SSIM_KERNEL_SOURCES:
-        with open(os.path.join(ROOT, "vmaf_float_vif_gb300", "csrc", n),
-                  "rb") as f:
-            h.update(f.read())
-    return h.hexdigest()[:16]
+    return source_hash(SSIM_KERNEL_SOURCES)
 
 
 def ssim_traffic(name):

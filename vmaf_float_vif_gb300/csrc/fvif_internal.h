@@ -14,18 +14,19 @@ constexpr int kScales = 4;
 constexpr int kMaxRadius = 64;               /* largest half-width accepted  */
 constexpr int kMaxTaps = 2 * kMaxRadius + 1; /* 129                          */
 
-/* Taps of one scale, handed to a launch by value (kernel parameter space),
- * so compile-time-indexed reads become constant-bank operands.            */
 constexpr int kMaxFixedTaps = 35; /* widest kernel compiled with fixed N */
 
+/* Taps of one scale, handed to a launch by value (kernel parameter space),
+ * so compile-time-indexed reads become constant-bank operands.            */
 struct Taps {
     float t[kMaxTaps];
     float2 t2[kMaxTaps]; /* (t[k], t[k]) for the packed two-lane operations */
     /* Vertical-pass taps for 16-bit integer samples s = x * 2^q (fixed
      * widths): t * x and t * (s * 2^-q) are the same real product, so
      * fl(t * x) = fl((t * 2^-q) * s); likewise fl(t * fl(x * x)) =
-     * fl((t * 2^-2q) * fl(s * s)) and the same for x * y.  The scale-0
-     * passes read the samples without rescaling them.                      */
+     * fl((t * 2^-2q) * fl(s * s)) and the same for x * y.  The passes
+     * over 16-bit samples (the scale-0 statistic and the first decimation)
+     * read them without rescaling.                                         */
     float2 ra2[kMaxFixedTaps]; /* (t 2^-q, t 2^-q)     for (x, y)           */
     float2 rb2[kMaxFixedTaps]; /* (t 2^-2q, t 2^-2q)   for (x*x, y*y)       */
     float rc[kMaxFixedTaps];   /* t 2^-2q              for x*y              */
