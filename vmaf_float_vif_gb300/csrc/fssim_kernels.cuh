@@ -573,8 +573,14 @@ ssim_decimate_u8_partials_kernel(const DecimateParams p)
  * their own rows, and chunk 0 mirrors its first k/2 columns.  The last
  * window of a row never leaves the row (w even), so the right edge needs no
  * mirror.  No shared memory, no barrier. */
+/* CTAs per SM the window kernel's register allocation must allow: 4
+ * (64 registers) against 3 at 76-80 registers measured 4-9% faster at
+ * k = 3 and 6, though k = 3, 5, 6, 7 then spill a few bytes. */
+#ifndef FSSIM_WIN_MINB
+#define FSSIM_WIN_MINB 4
+#endif
 template <typename T, int K>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, FSSIM_WIN_MINB)
 ssim_decimate_windows_kernel(const DecimateParams p)
 {
     static_assert(K >= 2 && K <= 8, "window kernel for k = 2..8");
