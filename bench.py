@@ -501,6 +501,7 @@ def run_ours(args):
             "unit": "TFLOP/s",
             "frac": achieved / alu_peak,
             "traffic": traffic,
+            "traffic_note": traffic_note(traffic, TRAFFIC_PATH, True),
             "per_unit": "%d fp32 ops per pixel (20 N + 60: a multiply and "
                         "an add per tap for five quantities in two passes, "
                         "plus the products, statistic, terms and log2)"
@@ -564,6 +565,16 @@ def ssim_kernel_hash():
     return source_hash(SSIM_KERNEL_SOURCES)
 
 
+def traffic_note(value, path, scaled):
+    rel = os.path.relpath(path, ROOT)
+    if value is None:
+        return ("null: %s holds no ncu capture taken on the current kernel "
+                "sources" % rel)
+    return ("dram__bytes_read.sum + dram__bytes_write.sum of one ncu capture "
+            "(%s)%s" % (rel, ", scaled to this launch's frames" if scaled
+                        else ""))
+
+
 def ssim_traffic(name):
     try:
         with open(SSIM_TRAFFIC_PATH) as f:
@@ -624,6 +635,8 @@ def ssim_decimate_lines(args, hbm_peak, hbm_src, cpu_baseline=True):
                 "unit": "GB/s", "frac": achieved / hbm_peak,
                 "peak_note": hbm_src,
                 "traffic": ssim_traffic(name),
+                "traffic_note": traffic_note(ssim_traffic(name),
+                                             SSIM_TRAFFIC_PATH, False),
                 "per_unit": "%d bytes per frame pair (samples read once, "
                             "fp32 planes written once)" % per_pair,
             },
