@@ -26,6 +26,10 @@
  * These are readings of the page: (a) scale 1 means no decimation; (b)
  * round() rounds the real quotient half away from zero; (c) bit depths 9, 11,
  * 13, 14 and 15 divide by 2^(bitdepth - 8), as 10, 12 and 16 do.
+ *
+ * Environment: FSSIM_KERNEL=general|windows forces the kernel that scales
+ * 2..8 on 16-byte rows use (the default picks per scale and sample size, as
+ * measured); every choice gives the same bits.
  */
 #ifndef FSSIM_H
 #define FSSIM_H

@@ -41,6 +41,12 @@
  *    enqueue).
  *  - FVIF_CHUNK=n: frames per chunk of device inputs (1..1024) instead of
  *    the default, read by fvif_create.
+ *  - FVIF_TERMS=fp64: the two log terms of every pixel are evaluated by the
+ *    fp64 sequence itself instead of fp32 pairs with an fp64 fallback (same
+ *    bits, much slower; a check of the pair path), read by fvif_create.
+ *  - FVIF_HOST_SLOTS=n (2..4, default 3) and FVIF_HOST_LANES=n (1..2,
+ *    default 2): staging slots and compute lanes of fvif_score_host, read
+ *    by fvif_create (tuning knobs; the defaults were measured best).
  *  - FVIF_FAIL_ALLOC=n: test hook, read by fvif_create: allocation n
  *    (0 = the first) of the context fails as if the device were out of
  *    memory, so every failure path can be exercised without exhausting
