@@ -215,3 +215,19 @@ def test_stray_context_pointers_are_rejected(L):
     assert L.fvif_get_taps(bogus, 0, taps, 64) == E
     L.fvif_destroy(bogus)            # a no-op
     L.fvif_destroy(None)
+
+
+def test_every_environment_variable_is_documented():
+    """Each variable the library reads is described in a public header."""
+    csrc = os.path.join(ROOT, "vmaf_float_vif_gb300", "csrc")
+    read = set()
+    for n in os.listdir(csrc):
+        if n.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, n)) as f:
+                read |= set(re.findall(r'getenv\("([A-Z0-9_]+)"\)', f.read()))
+    headers = ""
+    for n in os.listdir(os.path.join(ROOT, "include")):
+        with open(os.path.join(ROOT, "include", n)) as f:
+            headers += f.read()
+    assert read, "no getenv call found"
+    assert not [v for v in read if v not in headers], read
