@@ -1,0 +1,77 @@
+"""Register-spill audit of every kernel, from the assembler's own report
+(`-Xptxas -v`, cross-compiled here, no GPU).
+
+The VIF kernels are compiled to fit their register budgets (3 CTAs per SM
+for the fixed-width statistic, 2 for the 35-tap one on 16-bit samples)
+without spilling; a change that makes one spill fails here before any GPU
+run.  The float_ssim window kernels trade a few spilled bytes at k = 3, 5,
+6 and 7 for a fourth CTA per SM (measured faster); their budget is 32
+bytes of spill stores."""
+import os
+import re
+import shutil
+import subprocess
+from concurrent.futures import ThreadPoolExecutor
+
+import pytest
+
+from vmaf_float_vif_gb300 import _build
+
+SSIM_SPILL_BUDGET = 32
+
+
+@pytest.fixture(scope="module")
+def report(tmp_path_factory):
+    nvcc = _build._nvcc()
+    if not (os.path.exists(nvcc) or shutil.which(nvcc)):
+        pytest.skip("no CUDA toolkit on this machine")
+    out = tmp_path_factory.mktemp("audit")
+
+    def run(src):
+        r = subprocess.run([nvcc, *_build.NVCC_FLAGS, "-Xptxas", "-v", "-c",
+                            os.path.join(_build.CSRC, src), "-o",
+                            str(out / (src + ".o"))],
+                           capture_output=True, text=True)
+        assert r.returncode == 0, r.stderr[-2000:]
+        return r.stderr
+
+    with ThreadPoolExecutor(min(8, len(_build.SOURCES))) as ex:
+        logs = list(ex.map(run, _build.SOURCES))
+    kernels = {}
+    for log in logs:
+        fn = None
+        for line in log.splitlines():
+            m = re.search(r"Compiling entry function '(\S+)'", line)
+            if m:
+                fn = m.group(1)
+                kernels[fn] = {}
+            m = re.search(r"(\d+) bytes spill stores, (\d+) bytes spill "
+                          r"loads", line)
+            if m and fn:
+                kernels[fn]["spill_st"] = int(m.group(1))
+                kernels[fn]["spill"] = int(m.group(1)) + int(m.group(2))
+            m = re.search(r"Used (\d+) registers", line)
+            if m and fn:
+                kernels[fn]["regs"] = int(m.group(1))
+    return kernels
+
+
+def test_every_kernel_is_reported(report):
+    names = " ".join(report)
+    for k in ("stats_kernel", "decimate_kernel", "final_kernel",
+              "ssim_decimate_u8_partials_kernel",
+              "ssim_decimate_windows_kernel", "ssim_decimate_kernel"):
+        assert k in names, k
+    assert all("regs" in v and "spill" in v for v in report.values())
+
+
+def test_vif_kernels_do_not_spill(report):
+    bad = {k: v for k, v in report.items()
+           if "fvif" in k and v["spill"] > 0}
+    assert not bad, bad
+
+
+def test_ssim_kernels_within_spill_budget(report):
+    bad = {k: v for k, v in report.items()
+           if "fssim" in k and v["spill_st"] > SSIM_SPILL_BUDGET}
+    assert not bad, bad
