@@ -534,6 +534,53 @@ def pin_sum_order(L):
         assert det["scores"][s] == float(tn) / float(td), s
 
 
+def pin_row_sums_left_to_right(L):
+    """[A] Decision, "Three kernels per scale": a row's terms are added left
+    to right into one fp32 accumulator that starts at zero; [A] Context names
+    the same two-level sum among the four properties a twin must copy.  The
+    per-pixel terms are rebuilt from the oracle's decimated planes through
+    its filter and its term function (both pinned on their own above), the
+    products x*x, y*y, x*y rounded to fp32, and each row is then summed here
+    column by column, one fp32 rounding per add, and compared bit for bit
+    with the oracle's row sums.  The fixture is checked to tell the orders
+    apart: summing every row right to left must change at least one row."""
+    from vmaf_float_vif_gb300 import synthetic as S
+    case = S.custom_noise_case(200, 120, 8)
+    r, d = case.pair(0)
+    for ks in (0.5, 1.0):
+        det = oracle.frame(r, d, 8, ks, 2.0, detail=True, L=L)
+        told_apart = False
+        for s in range(4):
+            x, y = det["planes"][s]
+            tp = oracle.taps(ks, s, L=L)
+            mu1 = oracle.filter_plane(x, tp, L=L)
+            mu2 = oracle.filter_plane(y, tp, L=L)
+            fxx = oracle.filter_plane(np.float32(x) * np.float32(x), tp, L=L)
+            fyy = oracle.filter_plane(np.float32(y) * np.float32(y), tp, L=L)
+            fxy = oracle.filter_plane(np.float32(x) * np.float32(y), tp, L=L)
+            hs, ws = x.shape
+            num, den = oracle.pixel_terms(mu1.ravel(), mu2.ravel(),
+                                          fxx.ravel(), fyy.ravel(),
+                                          fxy.ravel(), 2.0, L=L)
+            num = num.reshape(hs, ws)
+            den = den.reshape(hs, ws)
+            fwd_n = np.zeros(hs, np.float32)
+            fwd_d = np.zeros(hs, np.float32)
+            rev_n = np.zeros(hs, np.float32)
+            for j in range(ws):
+                fwd_n = (fwd_n + num[:, j]).astype(np.float32)
+                fwd_d = (fwd_d + den[:, j]).astype(np.float32)
+                rev_n = (rev_n + num[:, ws - 1 - j]).astype(np.float32)
+            rows = det["rows"][s]
+            assert rows.dtype == np.float32
+            assert np.array_equal(rows[:, 0].view(np.uint32),
+                                  fwd_n.view(np.uint32)), (ks, s)
+            assert np.array_equal(rows[:, 1].view(np.uint32),
+                                  fwd_d.view(np.uint32)), (ks, s)
+            told_apart |= not np.array_equal(rev_n, fwd_n)
+        assert told_apart, "fixture does not distinguish the sum orders"
+
+
 def pin_gain_limit_option(L):
     """A gain limit of 1 caps g = 2 (dist = 2 ref) before the term and after
     sv: sv = 4 s1 - 2 (2 s1) -> eps, num = log2(1 + s1 / (eps + nsq))."""
@@ -584,5 +631,6 @@ ALL_PINS = [
     pin_log2_exact_powers, pin_log2_error_bound, pin_log2_monotone,
     pin_identical_frames, pin_black_frames_exactly_one,
     pin_flat_ref_closed_form, pin_textbook_vif, pin_sum_order,
+    pin_row_sums_left_to_right,
     pin_gain_limit_option, pin_options_and_debug,
 ]

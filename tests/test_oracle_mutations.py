@@ -55,6 +55,9 @@ MUTATIONS = [
      "scores[s] = (double)total_num / (double)total_den;",
      "scores[s] = (double)total_den / (double)total_num;",
      [pins.pin_textbook_vif, pins.pin_sum_order]),
+    ("row_sum_right_to_left", "for (int j = 0; j < ws; ++j) {",
+     "for (int j = ws - 1; j >= 0; --j) {",
+     [pins.pin_row_sums_left_to_right]),
     ("decimate_with_own_scale_taps", "fvo_decimate(x, ws, hs, taps[s + 1], ntaps[s + 1], nx);",
      "fvo_decimate(x, ws, hs, taps[s], ntaps[s], nx);",
      [pins.pin_textbook_vif]),
