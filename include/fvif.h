@@ -216,6 +216,23 @@ int fvif_profile_enable(fvif_ctx *ctx, int enable);
 int fvif_profile_read(fvif_ctx *ctx, int kind, double *total_ms,
                       long long *launches);
 
+/* Per-chunk timing of the last fvif_score_host call made while profiling
+ * was enabled (fvif_profile_enable), to show where a host-input call spends
+ * its time: returns the number of chunks n of that call (0 if none) and
+ * writes min(n, cap) rows of six doubles to out (HOST memory):
+ *   [0] copy start  : the chunk's host-to-device copy begins (its staging
+ *                     slot is free and the copy stream reaches it),
+ *   [1] copy end    : both of its planes are on the device,
+ *   [2] score start : its lane may start it (copy done, lane free),
+ *   [3] score end   : its scores are reduced,
+ * all device time in ms since chunk 0's copy start (CUDA events), and
+ *   [4], [5]        : host ms since the call began at which the library
+ *                     started and finished enqueueing the chunk.
+ * Waits for the recorded events.  Returns FVIF_EINVAL or FVIF_ECUDA on
+ * error.  "ADR-1444 ...", Consequences, breaks the exact twin's frame time
+ * down by measurement; this does the same for the host-input path. */
+int fvif_profile_host(fvif_ctx *ctx, double *out, int cap);
+
 /* Size in bytes of the fixed device scratch array used by
  * fvif_score_noalloc (8 MiB). */
 #define FVIF_NOALLOC_SCRATCH_BYTES (8u * 1024u * 1024u)
@@ -232,8 +249,12 @@ int fvif_profile_read(fvif_ctx *ctx, int kind, double *total_ms,
  * (NULL = legacy default stream) and the call returns without waiting.
  * Frames are scored one at a time through the same kernels as fvif_score,
  * with the intermediate planes and row sums kept in one file-scope device
- * array of FVIF_NOALLOC_SCRATCH_BYTES that the library holds on every GPU
- * where it is loaded, until the process exits.
+ * array of FVIF_NOALLOC_SCRATCH_BYTES.  CUDA loads the library's device
+ * code into a context lazily, so that array is taken from a device's memory
+ * by the first call of this function there, and is held until the context
+ * is destroyed or the process exits.  A caller with a fixed memory budget,
+ * or one that captures streams into graphs, makes one call at set-up time,
+ * before the budget is fixed and before any capture.
  *
  * Limit: a frame needs, rounding each part up to 256 bytes,
  * 8*(w1*h1) + 8*(w2*h2) + 8*(w3*h3) + 8*(h0+h1+h2+h3) bytes, where
@@ -241,9 +262,11 @@ int fvif_profile_read(fvif_ctx *ctx, int kind, double *total_ms,
  * rejected with FVIF_ETOOBIG before anything is launched (1920x1080 needs
  * about 5.5 MB and fits; 3840x2160 does not).
  *
- * The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress) with that device current; make that first call
- * before any stream capture.  Every call uses the same array and leaves its
+ * Every call looks up the array's device address in the current context
+ * (cudaGetSymbolAddress, a host-side lookup once the code is loaded), so
+ * the call stays right after cudaDeviceReset or a change of context.  All
+ * buffers must be on the current device.  Every call uses the same array and
+ * leaves its
  * last contents there; nothing in it needs to start at zero.  Calls whose
  * work overlaps on the GPU (different streams, or several host threads)
  * race on the array: serialise them, e.g. on one stream.

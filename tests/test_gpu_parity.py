@@ -2,9 +2,10 @@
 
 Bar: every score equal to the oracle's bits (the target is identity; the
 pages' parity gate of 5e-5 is the acceptance bound and is reported when a
-value differs).  Cases: every workload that the oracle finishes in seconds,
-in full; the 4K workloads at full size in the launch configuration the
-benchmark times, on sampled frames; edge frame sizes, bit depths,
+value differs).  Cases: every workload in full -- the 4K clip's 20 frames
+and the 240-frame 4K stream at each of its three kernelscales, in the launch
+configuration the benchmark times, every frame checked against the oracle
+(run on all host cores; a few minutes); edge frame sizes, bit depths,
 kernelscales (fixed-width and run-time-width kernels), noise variances,
 degenerate content, every API entry point and the per-step diagnostics.
 """
@@ -52,15 +53,14 @@ def test_workload_cases_bit_identical(fv, name, ks):
     assert_bitwise(got, want, "%s ks=%g" % (name, ks))
 
 
-def test_4k_8bit_full_clip_sampled(fv):
-    """All 20 frames of the 8-bit 4K clip in one call (two chunks); sampled
-    frames checked against the oracle one by one."""
+def test_4k_8bit_full_clip(fv):
+    """All 20 frames of the 8-bit 4K clip in one call, every frame against
+    the oracle."""
     case = S.CASES["c4_4k_8b"]
     ref, dist = case.batch(range(case.frames))
     got = gpu_scores(fv, case, ref, dist, 1.0, case.nsq)
-    for f in (0, 15, 16, 19):
-        want = oracle.frame(ref[f], dist[f], 8, 1.0, case.nsq)
-        assert_bitwise(got[f], want, "c4 frame %d" % f)
+    want = oracle_scores(ref, dist, 8, 1.0, case.nsq)
+    assert_bitwise(got, want, "c4 all %d frames" % case.frames)
 
 
 _STREAM = {}
@@ -74,11 +74,11 @@ def c5_stream():
 
 
 @pytest.mark.parametrize("ks", [0.5, 1.0, 2.0])
-def test_4k_10bit_stream_sampled(fv, ks):
+def test_4k_10bit_stream(fv, ks):
     """The 240-frame 10-bit 4K stream in the benchmark's launch
     configuration (device inputs, one fvif_score_async call, the context's
     default chunk: about 4096 scale-0 strips per launch, 31 frames at 4K);
-    sampled frames on both sides of chunk boundaries against the oracle."""
+    every frame against the oracle."""
     torch = torch_mod()
     case = S.CASES["c5_4k_10b"]
     ref, dist = c5_stream()
@@ -90,9 +90,8 @@ def test_4k_10bit_stream_sampled(fv, ks):
         ctx.score_async(r, d, out)
         torch.cuda.synchronize()
     got = out.cpu().numpy().reshape(-1, 4)
-    samples = [0, 17, 30, 31, 128, 239]
-    want = oracle_scores(ref[samples], dist[samples], 10, ks, case.nsq)
-    assert_bitwise(got[samples], want, "c5 ks=%g" % ks)
+    want = oracle_scores(ref, dist, 10, ks, case.nsq)
+    assert_bitwise(got, want, "c5 ks=%g, all %d frames" % (ks, case.frames))
     assert np.all((got > 0) & (got <= 1.0 + 1e-6))
 
 
@@ -227,6 +226,28 @@ def test_entry_points_agree(fv):
         assert_bitwise(got, want, "host pinned")
         # repeated calls reuse the buffers and keep the bits
         assert_bitwise(ctx.score_host(ref, dist), want, "host again")
+
+
+def test_host_path_chunk_timing(fv):
+    """fvif_profile_host: one row per chunk of the last profiled
+    fvif_score_host call (a quarter chunk first, then chunks of 16 frames),
+    with events in causal order; the scores keep their bits while timed."""
+    case = S.custom_noise_case(300, 170, 10, frames=37)
+    ref, dist = case.batch(range(case.frames))
+    want = oracle_scores(ref, dist, 10, 1.0, 2.0)
+    with fv.Context(case.w, case.h, 10, 1.0, 2.0) as ctx:
+        ctx.score_host(ref, dist)
+        assert ctx.profile_host().shape == (0, 6)
+        ctx.profile(True)
+        assert_bitwise(ctx.score_host(ref, dist), want, "host, profiled")
+        t = ctx.profile_host()
+        ctx.profile(False)
+    assert t.shape == (4, 6)      # 4 + 16 + 16 + 1 frames
+    c0, c1, s0, s1, h0, h1 = t.T
+    assert c0[0] == 0.0
+    assert np.all(c1 >= c0) and np.all(s0 >= c1) and np.all(s1 > s0)
+    assert np.all(c0[1:] >= c1[:-1])          # one copy stream, in order
+    assert np.all(h1 >= h0) and np.all(h0[1:] >= h1[:-1])
 
 
 def test_zero_frames_and_bad_calls(fv):

@@ -27,7 +27,8 @@ EXPORTS = (
     "fvif_create", "fvif_score", "fvif_score_async", "fvif_score_host",
     "fvif_destroy", "fvif_set_stream", "fvif_last_error", "fvif_strerror",
     "fvif_chunk_frames", "fvif_get_taps", "fvif_debug_frame",
-    "fvif_profile_enable", "fvif_profile_read", "fvif_score_noalloc",
+    "fvif_profile_enable", "fvif_profile_read", "fvif_profile_host",
+    "fvif_score_noalloc",
     "fvif_debug_terms", "fvif_default_options", "fvif_create_ex",
     "fvif_score_debug",
     # include/fssim.h
@@ -98,6 +99,8 @@ def _declare(L: ctypes.CDLL) -> ctypes.CDLL:
     L.fvif_profile_enable.restype = i
     L.fvif_profile_read.argtypes = [vp, i, dp, ctypes.POINTER(ctypes.c_longlong)]
     L.fvif_profile_read.restype = i
+    L.fvif_profile_host.argtypes = [vp, dp, i]
+    L.fvif_profile_host.restype = i
     L.fvif_default_options.argtypes = [ctypes.POINTER(FvifOptions)]
     L.fvif_default_options.restype = None
     L.fvif_create_ex.argtypes = [i, i, i, f, d, ctypes.POINTER(FvifOptions)]
@@ -364,6 +367,12 @@ def fvif_score_noalloc(ref, dist, out, w: int, h: int, bitdepth: int,
             not out.is_contiguous()):
         raise TypeError("out must be a contiguous CUDA float64 tensor of "
                         ">= 4*n values")
+    cur = torch.cuda.current_device()
+    for name, t in (("ref", ref), ("dist", dist), ("out", out)):
+        if isinstance(t, torch.Tensor) and t.is_cuda and t.device.index != cur:
+            raise ValueError("%s is on cuda:%d but the current device is "
+                             "cuda:%d: the scratch array used is the current "
+                             "device's" % (name, t.device.index, cur))
     handle = getattr(stream, "cuda_stream", stream)
     st = lib().fvif_score_noalloc(int(w), int(h), int(bitdepth),
                                   float(kernelscale), float(sigma_nsq),
@@ -389,6 +398,26 @@ def fvif_profile_read(ctx: int, kind: int):
     if st:
         raise FvifError(st, "fvif_profile_read")
     return ms.value, n.value
+
+
+HOST_PROFILE_COLUMNS = ("copy_start", "copy_end", "score_start",
+                        "score_end", "enqueue_start", "enqueue_end")
+
+
+def fvif_profile_host(ctx: int) -> np.ndarray:
+    """Per-chunk timing of the last fvif_score_host call made while
+    profiling: an (n, 6) array with the columns HOST_PROFILE_COLUMNS (device
+    ms since chunk 0's copy start, then host ms since the call began)."""
+    n = lib().fvif_profile_host(ctx, None, 0)
+    if n < 0:
+        raise FvifError(n, "fvif_profile_host")
+    out = np.zeros((n, 6), np.float64)
+    if n:
+        got = lib().fvif_profile_host(
+            ctx, out.ctypes.data_as(ctypes.POINTER(ctypes.c_double)), n)
+        if got < 0:
+            raise FvifError(got, "fvif_profile_host")
+    return out
 
 
 def fvif_debug_terms(ctx: int, mu1, mu2, xx, yy, xy, count_fallbacks=True):
@@ -538,6 +567,11 @@ class Context:
 
     def profile(self, enable: bool = True) -> None:
         fvif_profile_enable(self.handle, enable)
+
+    def profile_host(self) -> np.ndarray:
+        """Per-chunk timing of the last profiled score_host call (see
+        fvif_profile_host)."""
+        return fvif_profile_host(self.handle)
 
     def profile_read(self):
         """{kind name: (total ms, launches)}"""

@@ -221,6 +221,18 @@ struct fvif_ctx {
     cudaEvent_t copied[kMaxStage] = {};
     cudaEvent_t consumed[kMaxStage] = {};
 
+    /* per-chunk timing of the last fvif_score_host call made while
+     * profiling: the copy of each chunk on the copy stream, its scoring on
+     * its lane (from the moment the lane may start it to the end of its
+     * reduction), and the host time spent enqueueing it */
+    struct HostChunk {
+        cudaEvent_t copy0 = nullptr, copy1 = nullptr;
+        cudaEvent_t score0 = nullptr, score1 = nullptr;
+        double enq0 = 0.0, enq1 = 0.0; /* host ms since the call began */
+    };
+    std::vector<HostChunk> host_prof;
+    int host_prof_n = 0;
+
     size_t sample_bytes() const { return bitdepth == 8 ? 1u : 2u; }
     size_t frame_stride = 0; /* samples between consecutive input frames */
     size_t plane_bytes() const { return (size_t)w * h * sample_bytes(); }
@@ -318,6 +330,31 @@ void release(fvif_ctx *c)
     for (int k = 0; k < FVIF_K_COUNT; ++k)
         for (cudaEvent_t ev : c->prof_events[k])
             cudaEventDestroy(ev);
+    for (fvif_ctx::HostChunk &h : c->host_prof)
+        for (cudaEvent_t ev : {h.copy0, h.copy1, h.score0, h.score1})
+            if (ev)
+                cudaEventDestroy(ev);
+}
+
+/* The timing events of host-path chunk i, made on first use. */
+cudaError_t host_chunk_events(fvif_ctx *c, int i, fvif_ctx::HostChunk **out)
+{
+    while ((int)c->host_prof.size() <= i) {
+        fvif_ctx::HostChunk h;
+        cudaError_t e = cudaSuccess;
+        for (cudaEvent_t *ev : {&h.copy0, &h.copy1, &h.score0, &h.score1})
+            if (e == cudaSuccess)
+                e = cudaEventCreate(ev);
+        if (e != cudaSuccess) {
+            for (cudaEvent_t ev : {h.copy0, h.copy1, h.score0, h.score1})
+                if (ev)
+                    cudaEventDestroy(ev);
+            return e;
+        }
+        c->host_prof.push_back(h);
+    }
+    *out = &c->host_prof[i];
+    return cudaSuccess;
 }
 
 /* Record the start event of one launch of kind k (profiling only). */
@@ -842,8 +879,10 @@ int fvif_profile_enable(fvif_ctx *ctx, int enable)
 int fvif_profile_read(fvif_ctx *ctx, int kind, double *total_ms,
                       long long *launches)
 {
-    if (!ctx || kind < 0 || kind >= FVIF_K_COUNT || !total_ms || !launches)
-        return ctx ? set_status(ctx, FVIF_EINVAL) : FVIF_EINVAL;
+    if (!live(ctx))
+        return FVIF_EINVAL;
+    if (kind < 0 || kind >= FVIF_K_COUNT || !total_ms || !launches)
+        return set_status(ctx, FVIF_EINVAL);
     DeviceGuard g(ctx->device);
     double ms = 0.0;
     const std::vector<cudaEvent_t> &v = ctx->prof_events[kind];
@@ -858,6 +897,35 @@ int fvif_profile_read(fvif_ctx *ctx, int kind, double *total_ms,
     *total_ms = ms;
     *launches = ctx->launches[kind];
     return set_status(ctx, FVIF_OK);
+}
+
+int fvif_profile_host(fvif_ctx *ctx, double *out, int cap)
+{
+    if (!live(ctx))
+        return FVIF_EINVAL;
+    if (cap < 0 || (cap > 0 && !out))
+        return set_status(ctx, FVIF_EINVAL);
+    DeviceGuard g(ctx->device);
+    if (!g.ok)
+        return set_status(ctx, FVIF_ECUDA);
+    const int n = ctx->host_prof_n;
+    for (int i = 0; i < n && i < cap; ++i) {
+        const fvif_ctx::HostChunk &h = ctx->host_prof[i];
+        const cudaEvent_t evs[4] = {h.copy0, h.copy1, h.score0, h.score1};
+        for (int k = 0; k < 4; ++k) {
+            float t = 0.0f;
+            cudaError_t e = cudaEventSynchronize(evs[k]);
+            if (e == cudaSuccess)
+                e = cudaEventElapsedTime(&t, ctx->host_prof[0].copy0, evs[k]);
+            if (e != cudaSuccess)
+                return set_status(ctx, cuda_status(e));
+            out[6 * i + k] = t;
+        }
+        out[6 * i + 4] = h.enq0;
+        out[6 * i + 5] = h.enq1;
+    }
+    set_status(ctx, FVIF_OK);
+    return n;
 }
 
 int fvif_chunk_frames(const fvif_ctx *ctx)
@@ -969,6 +1037,10 @@ static int score_host_impl(fvif_ctx *ctx, const void *ref, const void *dist,
     const size_t pb = ctx->plane_bytes();
     const int hc = ctx->host_chunk;
     const size_t half = pb * (size_t)hc;
+    const bool prof = ctx->profiling;
+    const auto t_call = std::chrono::steady_clock::now();
+    if (prof)
+        ctx->host_prof_n = 0;
     cudaError_t e = fork_lanes(ctx);
     /* The first chunk is a quarter chunk: scoring starts once it has been
      * copied instead of waiting for a whole chunk to cross the host link. */
@@ -984,8 +1056,17 @@ static int score_host_impl(fvif_ctx *ctx, const void *ref, const void *dist,
         fvif_ctx::Lane &lane = ctx->lanes[i % ctx->host_lanes];
         unsigned char *dref = ctx->stage[slot];
         unsigned char *ddist = ctx->stage[slot] + half;
+        fvif_ctx::HostChunk *hp = nullptr;
+        if (prof) {
+            e = host_chunk_events(ctx, i, &hp);
+            if (e != cudaSuccess)
+                break;
+            hp->enq0 = ms_since(t_call);
+        }
         /* the slot is free once the chunk that used it last was scored */
         e = cudaStreamWaitEvent(ctx->copy_stream, ctx->consumed[slot], 0);
+        if (e == cudaSuccess && prof)
+            e = cudaEventRecord(hp->copy0, ctx->copy_stream);
         if (e == cudaSuccess)
             e = cudaMemcpy2DAsync(dref, pb,
                                   static_cast<const unsigned char *>(ref) +
@@ -998,10 +1079,14 @@ static int score_host_impl(fvif_ctx *ctx, const void *ref, const void *dist,
                                       fb * f0,
                                   fb, pb, nf, cudaMemcpyHostToDevice,
                                   ctx->copy_stream);
+        if (e == cudaSuccess && prof)
+            e = cudaEventRecord(hp->copy1, ctx->copy_stream);
         if (e == cudaSuccess)
             e = cudaEventRecord(ctx->copied[slot], ctx->copy_stream);
         if (e == cudaSuccess)
             e = cudaStreamWaitEvent(lane.stream, ctx->copied[slot], 0);
+        if (e == cudaSuccess && prof)
+            e = cudaEventRecord(hp->score0, lane.stream);
         if (e != cudaSuccess)
             break;
         st = run_chunk(ctx, lane, dref, ddist, nf,
@@ -1009,7 +1094,14 @@ static int score_host_impl(fvif_ctx *ctx, const void *ref, const void *dist,
                        (size_t)ctx->w * ctx->h);
         if (st != FVIF_OK)
             break;
-        e = cudaEventRecord(ctx->consumed[slot], lane.stream);
+        if (prof)
+            e = cudaEventRecord(hp->score1, lane.stream);
+        if (e == cudaSuccess)
+            e = cudaEventRecord(ctx->consumed[slot], lane.stream);
+        if (prof) {
+            hp->enq1 = ms_since(t_call);
+            ctx->host_prof_n = i + 1;
+        }
     }
     const cudaError_t ej = join_lanes(ctx);
     if (e != cudaSuccess || st != FVIF_OK || ej != cudaSuccess) {

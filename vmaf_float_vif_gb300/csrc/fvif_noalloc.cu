@@ -13,11 +13,12 @@
  * fixed array compiled into the library and uses the caller's input and
  * output buffers as they are.
  *
- * The array lives for as long as the library is loaded, on every GPU where
- * the library's device code is loaded, whether or not this entry point is
- * ever called.
+ * The array belongs to this file's device module.  CUDA loads a module into
+ * a context lazily by default, so the 8 MiB are taken from a device the first
+ * time this entry point runs there (the address lookup below loads the
+ * module), and are then held until the context is destroyed or the process
+ * exits.  A caller with a fixed budget makes one call at set-up time.
  */
-#include <mutex>
 
 #include "../../include/fvif.h"
 #include "fvif_internal.h"
@@ -31,36 +32,21 @@ namespace {
 static __device__ __align__(256) unsigned char
     g_noalloc_scratch[FVIF_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-
-struct DeviceScratch {
-    bool ready = false;
-    unsigned char *ptr = nullptr;
-};
-
-std::mutex g_setup_mutex;
-DeviceScratch g_devices[kMaxDevices];
-
 size_t align256(size_t n) { return (n + 255u) & ~(size_t)255u; }
 
-/* Device address of the scratch array on the current device, looked up
- * once per device (cudaGetSymbolAddress, with that device current). */
+/* Device address of the scratch array in the current context.  Host code
+ * cannot use the array's name as a device pointer, so the address is looked
+ * up with cudaGetSymbolAddress.  The lookup is repeated on every call: it is
+ * a host-side table lookup once the module is loaded, and it stays right
+ * after cudaDeviceReset or when the caller switches contexts, where an
+ * address kept from an earlier context would no longer be mapped. */
 int scratch_address(unsigned char **out)
 {
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess ||
+        p == nullptr)
         return FVIF_ECUDA;
-    std::lock_guard<std::mutex> lock(g_setup_mutex);
-    DeviceScratch &d = g_devices[dev];
-    if (!d.ready) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess ||
-            p == nullptr)
-            return FVIF_ECUDA;
-        d.ptr = static_cast<unsigned char *>(p);
-        d.ready = true;
-    }
-    *out = d.ptr;
+    *out = static_cast<unsigned char *>(p);
     return FVIF_OK;
 }
 
