@@ -47,6 +47,15 @@
  *  - FVIF_HOST_SLOTS=n (2..4, default 3) and FVIF_HOST_LANES=n (1..2,
  *    default 2): staging slots and compute lanes of fvif_score_host, read
  *    by fvif_create (tuning knobs; the defaults were measured best).
+ *  - FVIF_DEC_TMA=0: the first decimation (integer samples to scale 1)
+ *    loads its samples directly from global memory instead of staging each
+ *    tile in shared memory by tensor copies (same bits; read once per
+ *    process).  Staging is used when a frame's rows and the distance
+ *    between frames are multiples of 16 bytes and the planes start on a
+ *    16-byte boundary; a staged tile that has not arrived within one
+ *    second makes its CTA give up and the next synchronous call on the
+ *    context (fvif_score, fvif_score_host, fvif_score_debug) return
+ *    FVIF_ECUDA.
  *  - FVIF_FAIL_ALLOC=n: test hook, read by fvif_create: allocation n
  *    (0 = the first) of the context fails as if the device were out of
  *    memory, so every failure path can be exercised without exhausting
@@ -219,7 +228,7 @@ int fvif_profile_read(fvif_ctx *ctx, int kind, double *total_ms,
 /* Per-chunk timing of the last fvif_score_host call made while profiling
  * was enabled (fvif_profile_enable), to show where a host-input call spends
  * its time: returns the number of chunks n of that call (0 if none) and
- * writes min(n, cap) rows of six doubles to out (HOST memory):
+ * writes min(n, cap) rows of seven doubles to out (HOST memory):
  *   [0] copy start  : the chunk's host-to-device copy begins (its staging
  *                     slot is free and the copy stream reaches it),
  *   [1] copy end    : both of its planes are on the device,
@@ -227,11 +236,27 @@ int fvif_profile_read(fvif_ctx *ctx, int kind, double *total_ms,
  *   [3] score end   : its scores are reduced,
  * all device time in ms since chunk 0's copy start (CUDA events), and
  *   [4], [5]        : host ms since the call began at which the library
- *                     started and finished enqueueing the chunk.
+ *                     started and finished enqueueing the chunk,
+ *   [6]             : 1 if both of the chunk's input ranges were
+ *                     page-locked for this process's CUDA runtime, else 0.
  * Waits for the recorded events.  Returns FVIF_EINVAL or FVIF_ECUDA on
  * error.  "ADR-1444 ...", Consequences, breaks the exact twin's frame time
  * down by measurement; this does the same for the host-input path. */
 int fvif_profile_host(fvif_ctx *ctx, double *out, int cap);
+
+/* Measured throughput of separately rounded fp32 multiplies and adds on
+ * the current device, the operations the statistic is bound by ("ADR-1444
+ * ...", Decision: every operation that rounds is written as one rounded
+ * operation, so none is fused).  Runs one probe kernel on cuda_stream (NULL
+ * = legacy default stream) in which every thread of 4 CTAs per SM steps 8
+ * independent chains acc = acc * a + b (one rounded multiply, one rounded
+ * add) iters times, as scalar operations (packed == 0) or as the packed
+ * two-lane forms the filters use (packed != 0); waits for it and returns
+ * the operation count in *ops and the event-timed duration in *ms.
+ * Diagnostics for the roofline; allocates nothing.  FVIF_EINVAL for
+ * iters <= 0 or NULL outputs, FVIF_ECUDA on a CUDA error. */
+int fvif_alu_probe(int packed, long long iters, void *cuda_stream,
+                   double *ops, double *ms);
 
 /* Size in bytes of the fixed device scratch array used by
  * fvif_score_noalloc (8 MiB). */

@@ -121,6 +121,67 @@ def test_bit_depths(fv, bd, ks):
     assert_bitwise(got, want, "bitdepth %d ks=%g" % (bd, ks))
 
 
+@pytest.mark.parametrize("bd", [8, 9, 10, 12, 14, 16])
+@pytest.mark.parametrize("ks", [0.5, 1.0, 2.0])
+def test_bit_depths_staged_decimation(fv, bd, ks):
+    """Rows a multiple of 16 bytes long (192 samples): the first decimation
+    stages its source tiles in shared memory by tensor copies (the 180-wide
+    frames above take the direct loads); several tiles across and down,
+    ragged last tiles, every fixed width (5, 9 and 19 taps)."""
+    case = S.custom_noise_case(192, 140, bd, frames=2, seed=bd)
+    ref, dist = case.batch(range(2))
+    got = gpu_scores(fv, case, ref, dist, ks, 2.0)
+    want = oracle_scores(ref, dist, bd, ks, 2.0)
+    assert_bitwise(got, want, "bitdepth %d ks=%g (staged)" % (bd, ks))
+
+
+PLAIN_DECIMATION_CHILD = r"""
+import json, os, sys
+import numpy as np
+sys.path.insert(0, %(root)r)
+sys.path.insert(0, os.path.join(%(root)r, "tests"))
+import vmaf_float_vif_gb300 as fv
+from gpu_util import to_device
+z = np.load(%(inp)r)
+res = []
+for key, w, h, bd in %(cases)r:
+    ref, dist = z[key + "_r"], z[key + "_d"]
+    with fv.Context(w, h, bd, 1.0, 2.0) as ctx:
+        res.append(ctx.score(to_device(ref), to_device(dist)).tolist())
+print(json.dumps(res))
+"""
+
+
+def test_direct_load_decimation_in_child(fv, tmp_path):
+    """FVIF_DEC_TMA=0 makes the first decimation load its samples directly
+    (the variant every frame whose rows are not a multiple of 16 bytes
+    takes); on frames that would otherwise be staged it must give the same
+    bits, checked in a child process against the oracle."""
+    import json
+    import subprocess
+    import sys
+    cases = [("a", 576, 324, 8), ("b", 192, 140, 10), ("c", 256, 96, 16)]
+    arrays, want = {}, []
+    for key, w, h, bd in cases:
+        case = S.custom_noise_case(w, h, bd, frames=2, seed=len(key) + w)
+        r, d = case.batch(range(2))
+        arrays[key + "_r"], arrays[key + "_d"] = r, d
+        want.append(oracle_scores(r, d, bd, 1.0, 2.0))
+    inp = str(tmp_path / "frames.npz")
+    np.savez(inp, **arrays)
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    code = PLAIN_DECIMATION_CHILD % {"root": root, "inp": inp,
+                                     "cases": cases}
+    env = dict(os.environ, FVIF_DEC_TMA="0")
+    out = subprocess.run([sys.executable, "-c", code], env=env,
+                         capture_output=True, text=True, timeout=600)
+    assert out.returncode == 0, out.stderr[-2000:]
+    got = json.loads(out.stdout.strip().splitlines()[-1])
+    for (key, w, h, bd), g, wnt in zip(cases, got, want):
+        assert_bitwise(np.array(g), wnt, "direct loads %dx%d %d-bit" %
+                       (w, h, bd))
+
+
 @pytest.mark.parametrize("bd", [10, 16])
 def test_full_range_samples(fv, bd):
     """Samples at 0 and at the top code of the bit depth, next to each
@@ -237,13 +298,21 @@ def test_host_path_chunk_timing(fv):
     want = oracle_scores(ref, dist, 10, 1.0, 2.0)
     with fv.Context(case.w, case.h, 10, 1.0, 2.0) as ctx:
         ctx.score_host(ref, dist)
-        assert ctx.profile_host().shape == (0, 6)
+        assert ctx.profile_host().shape == (0, 7)
         ctx.profile(True)
         assert_bitwise(ctx.score_host(ref, dist), want, "host, profiled")
         t = ctx.profile_host()
+        torch = torch_mod()
+        pr = torch.from_numpy(ref.view(np.int16)).pin_memory()
+        pd = torch.from_numpy(dist.view(np.int16)).pin_memory()
+        assert_bitwise(ctx.score_host(pr.numpy().view(np.uint16),
+                                      pd.numpy().view(np.uint16)), want,
+                       "host pinned, profiled")
+        tp = ctx.profile_host()
         ctx.profile(False)
-    assert t.shape == (4, 6)      # 4 + 16 + 16 + 1 frames
-    c0, c1, s0, s1, h0, h1 = t.T
+    assert t.shape == (4, 7)      # 4 + 16 + 16 + 1 frames
+    assert np.all(t[:, 6] == 0.0) and np.all(tp[:, 6] == 1.0)
+    c0, c1, s0, s1, h0, h1, _ = t.T
     assert c0[0] == 0.0
     assert np.all(c1 >= c0) and np.all(s0 >= c1) and np.all(s1 > s0)
     assert np.all(c0[1:] >= c1[:-1])          # one copy stream, in order

@@ -199,6 +199,10 @@ struct fvif_ctx {
     int rows_base[kScales] = {};
     float2 *sums = nullptr;      /* chunk x 4 (diagnostics)               */
 
+    /* bit 0 set by a decimation whose staged source tile did not arrive
+     * within its wait limit; read and cleared by the synchronous calls   */
+    unsigned *d_status = nullptr;
+    unsigned *h_status = nullptr; /* pinned copy of d_status             */
     double *d_out = nullptr;     /* results of the synchronous calls      */
     double *h_out = nullptr;     /* pinned staging of d_out               */
     int out_cap = 0;
@@ -229,6 +233,7 @@ struct fvif_ctx {
         cudaEvent_t copy0 = nullptr, copy1 = nullptr;
         cudaEvent_t score0 = nullptr, score1 = nullptr;
         double enq0 = 0.0, enq1 = 0.0; /* host ms since the call began */
+        double locked = 0.0; /* 1: both input ranges page-locked       */
     };
     std::vector<HostChunk> host_prof;
     int host_prof_n = 0;
@@ -316,6 +321,10 @@ void release(fvif_ctx *c)
         cudaEventDestroy(c->fork);
     if (c->sums)
         cudaFree(c->sums);
+    if (c->d_status)
+        cudaFree(c->d_status);
+    if (c->h_status)
+        cudaFreeHost(c->h_status);
     if (c->d_out)
         cudaFree(c->d_out);
     if (c->h_out)
@@ -433,6 +442,7 @@ int run_chunk(fvif_ctx *c, fvif_ctx::Lane &l, const void *ref,
         d.nframes = nf;
         d.dst = l.pyr[s];
         d.dst_frame_elems = (size_t)c->ws[s] * c->hs[s];
+        d.status = c->d_status;
         e = prof_begin(c, FVIF_K_DECIMATE, st);
         if (e == cudaSuccess)
             e = launch_decimate(d, c->taps[s], st);
@@ -592,15 +602,40 @@ int ensure_debug(fvif_ctx *c, int n)
     return FVIF_OK;
 }
 
+/* Enqueue the read of the context's device status word (after the work
+ * queued on the context stream). */
+cudaError_t status_to_host(fvif_ctx *c)
+{
+    return cudaMemcpyAsync(c->h_status, c->d_status, sizeof(unsigned),
+                           cudaMemcpyDeviceToHost, c->stream);
+}
+
+/* After the stream is synchronised: FVIF_ECUDA if a kernel marked the
+ * status word (which is then cleared for the next call), else FVIF_OK. */
+int status_check(fvif_ctx *c)
+{
+    if (*c->h_status == 0)
+        return FVIF_OK;
+    *c->h_status = 0;
+    cudaMemsetAsync(c->d_status, 0, sizeof(unsigned), c->stream);
+    cudaStreamSynchronize(c->stream);
+    return FVIF_ECUDA;
+}
+
 int finish_to_host(fvif_ctx *c, int n, double *out)
 {
     cudaError_t e = cudaMemcpyAsync(c->h_out, c->d_out,
                                     sizeof(double) * kScales * (size_t)n,
                                     cudaMemcpyDeviceToHost, c->stream);
     if (e == cudaSuccess)
+        e = status_to_host(c);
+    if (e == cudaSuccess)
         e = cudaStreamSynchronize(c->stream);
     if (e != cudaSuccess)
         return cuda_status(e);
+    const int st = status_check(c);
+    if (st != FVIF_OK)
+        return st;
     std::memcpy(out, c->h_out, sizeof(double) * kScales * (size_t)n);
     return FVIF_OK;
 }
@@ -801,6 +836,14 @@ static fvif_ctx *create_ex_impl(int w, int h, int bitdepth, float kernelscale,
     if (e == cudaSuccess)
         e = ctx_malloc(c, (void **)&c->sums,
                        sizeof(float2) * kScales * (size_t)c->chunk);
+    if (e == cudaSuccess)
+        e = ctx_malloc(c, (void **)&c->d_status, sizeof(unsigned));
+    if (e == cudaSuccess)
+        e = ctx_malloc_host(c, (void **)&c->h_status, sizeof(unsigned));
+    if (e == cudaSuccess) {
+        *c->h_status = 0;
+        e = cudaMemset(c->d_status, 0, sizeof(unsigned));
+    }
     int st = cuda_status(e);
     if (st == FVIF_OK)
         st = ensure_out(c, c->chunk);
@@ -919,10 +962,11 @@ int fvif_profile_host(fvif_ctx *ctx, double *out, int cap)
                 e = cudaEventElapsedTime(&t, ctx->host_prof[0].copy0, evs[k]);
             if (e != cudaSuccess)
                 return set_status(ctx, cuda_status(e));
-            out[6 * i + k] = t;
+            out[7 * i + k] = t;
         }
-        out[6 * i + 4] = h.enq0;
-        out[6 * i + 5] = h.enq1;
+        out[7 * i + 4] = h.enq0;
+        out[7 * i + 5] = h.enq1;
+        out[7 * i + 6] = h.locked;
     }
     set_status(ctx, FVIF_OK);
     return n;
@@ -1005,12 +1049,36 @@ static int score_debug_impl(fvif_ctx *ctx, const void *ref, const void *dist,
                             sizeof(double) * 15 * (size_t)n_frames,
                             cudaMemcpyDeviceToHost, ctx->stream);
     if (st == FVIF_OK && e == cudaSuccess)
+        e = status_to_host(ctx);
+    if (st == FVIF_OK && e == cudaSuccess)
         e = cudaStreamSynchronize(ctx->stream);
     if (st == FVIF_OK && e != cudaSuccess)
         st = cuda_status(e);
     if (st == FVIF_OK)
+        st = status_check(ctx);
+    if (st == FVIF_OK)
         std::memcpy(out, ctx->h_debug, sizeof(double) * 15 * (size_t)n_frames);
     return set_status(ctx, st);
+}
+
+/* Whether host range [p, p + n) is page-locked (allocated by
+ * cudaHostAlloc / cudaMallocHost or registered with cudaHostRegister), as
+ * this process's CUDA runtime sees it: both ends are checked.  Clears the
+ * error a pageable pointer leaves behind on older runtimes. */
+static bool page_locked(const void *p, size_t n)
+{
+    for (const unsigned char *q :
+         {static_cast<const unsigned char *>(p),
+          static_cast<const unsigned char *>(p) + (n ? n - 1 : 0)}) {
+        cudaPointerAttributes a;
+        if (cudaPointerGetAttributes(&a, q) != cudaSuccess) {
+            cudaGetLastError();
+            return false;
+        }
+        if (a.type != cudaMemoryTypeHost)
+            return false;
+    }
+    return true;
 }
 
 static int score_host_impl(fvif_ctx *ctx, const void *ref, const void *dist,
@@ -1063,22 +1131,35 @@ static int score_host_impl(fvif_ctx *ctx, const void *ref, const void *dist,
                 break;
             hp->enq0 = ms_since(t_call);
         }
+        const unsigned char *href =
+            static_cast<const unsigned char *>(ref) + fb * f0;
+        const unsigned char *hdist =
+            static_cast<const unsigned char *>(dist) + fb * f0;
+        if (prof)
+            hp->locked = page_locked(href, fb * (nf - 1) + pb) &&
+                                 page_locked(hdist, fb * (nf - 1) + pb)
+                             ? 1.0
+                             : 0.0;
         /* the slot is free once the chunk that used it last was scored */
         e = cudaStreamWaitEvent(ctx->copy_stream, ctx->consumed[slot], 0);
         if (e == cudaSuccess && prof)
             e = cudaEventRecord(hp->copy0, ctx->copy_stream);
+        /* packed luma planes: one plain copy per plane set; planes further
+         * apart (planar YUV frames): one 2-D copy that skips the chroma */
         if (e == cudaSuccess)
-            e = cudaMemcpy2DAsync(dref, pb,
-                                  static_cast<const unsigned char *>(ref) +
-                                      fb * f0,
-                                  fb, pb, nf, cudaMemcpyHostToDevice,
-                                  ctx->copy_stream);
+            e = fb == pb ? cudaMemcpyAsync(dref, href, pb * nf,
+                                           cudaMemcpyHostToDevice,
+                                           ctx->copy_stream)
+                         : cudaMemcpy2DAsync(dref, pb, href, fb, pb, nf,
+                                             cudaMemcpyHostToDevice,
+                                             ctx->copy_stream);
         if (e == cudaSuccess)
-            e = cudaMemcpy2DAsync(ddist, pb,
-                                  static_cast<const unsigned char *>(dist) +
-                                      fb * f0,
-                                  fb, pb, nf, cudaMemcpyHostToDevice,
-                                  ctx->copy_stream);
+            e = fb == pb ? cudaMemcpyAsync(ddist, hdist, pb * nf,
+                                           cudaMemcpyHostToDevice,
+                                           ctx->copy_stream)
+                         : cudaMemcpy2DAsync(ddist, pb, hdist, fb, pb, nf,
+                                             cudaMemcpyHostToDevice,
+                                             ctx->copy_stream);
         if (e == cudaSuccess && prof)
             e = cudaEventRecord(hp->copy1, ctx->copy_stream);
         if (e == cudaSuccess)

@@ -1,8 +1,120 @@
 /* Decimation kernels, the per-(frame, scale) final reduction and the plane
  * unpacking used by the diagnostics entry point. */
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+#include <cstdlib>
+#include <mutex>
+
+#include "fvif_dec_tma.cuh"
 #include "fvif_dispatch.cuh"
 
 namespace fvif {
+
+namespace {
+
+/* cuTensorMapEncodeTiled from the driver, looked up once through the
+ * runtime (no link-time dependency on the driver library). */
+PFN_cuTensorMapEncodeTiled_v12000 encode_tiled()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p,
+                                             12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+        else
+            cudaGetLastError();
+    });
+    return fn;
+}
+
+/* FVIF_DEC_TMA=0 in the environment: the first decimation loads its
+ * samples directly (decimate_kernel) instead of staging them by tensor
+ * copies (same bits). */
+bool dec_tma_enabled()
+{
+    static const bool on = [] {
+        const char *e = std::getenv("FVIF_DEC_TMA");
+        return !(e && std::atoi(e) == 0);
+    }();
+    return on;
+}
+
+/* A 3-D tensor map over n frames of one plane of integer samples: x (the
+ * row, contiguous), y (rows, w apart), z (frames, frame_elems apart), with
+ * the box of one decimation tile. */
+bool make_plane_map(CUtensorMap *m, const void *base, SrcKind k, int w, int h,
+                    int n, size_t frame_elems, int box_w, int box_h)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_tiled();
+    if (!enc)
+        return false;
+    const size_t eb = k == SrcKind::U8 ? 1 : 2;
+    const cuuint64_t dims[3] = {(cuuint64_t)w, (cuuint64_t)h, (cuuint64_t)n};
+    const cuuint64_t strides[2] = {(cuuint64_t)(w * eb),
+                                   (cuuint64_t)(frame_elems * eb)};
+    const cuuint32_t box[3] = {(cuuint32_t)box_w, (cuuint32_t)box_h, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(m,
+               k == SrcKind::U8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                : CU_TENSOR_MAP_DATA_TYPE_UINT16,
+               3, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+/* The staged variant serves a launch when: a status word is given, the
+ * widths are fixed, the planes meet the tensor-copy rules (16-byte aligned
+ * bases, rows and frames a multiple of 16 bytes apart) and are at least
+ * 2R + 2 samples on each side (then every reflected index a kept output
+ * needs lies inside its tile). */
+template <int N, SrcKind K>
+bool dec_tma_fits(const DecArgs &a)
+{
+    constexpr size_t eb = K == SrcKind::U8 ? 1 : 2;
+    constexpr int r = N / 2;
+    return a.status && dec_tma_enabled() && a.w >= 2 * r + 2 &&
+           a.h >= 2 * r + 2 && (a.w * eb) % 16 == 0 &&
+           (a.src.frame_elems * eb) % 16 == 0 &&
+           reinterpret_cast<uintptr_t>(a.src.x) % 16 == 0 &&
+           reinterpret_cast<uintptr_t>(a.src.y) % 16 == 0;
+}
+
+template <int N, SrcKind K>
+cudaError_t run_decimate_tma(const DecArgs &a, const Taps &tp,
+                             cudaStream_t st, bool *used)
+{
+    *used = false;
+    constexpr int eb = K == SrcKind::U8 ? 1 : 2;
+    constexpr int r = N / 2;
+    if (!dec_tma_fits<N, K>(a))
+        return cudaSuccess;
+    CUtensorMap mx, my;
+    if (!make_plane_map(&mx, a.src.x, K, a.w, a.h, a.nframes,
+                        a.src.frame_elems, dtma_bw(r, eb), dtma_bh(r)) ||
+        !make_plane_map(&my, a.src.y, K, a.w, a.h, a.nframes,
+                        a.src.frame_elems, dtma_bw(r, eb), dtma_bh(r)))
+        return cudaSuccess;
+    static bool done[64];
+    const size_t bytes = dtma_smem_bytes(r, eb);
+    cudaError_t e = ensure_smem(decimate_tma_kernel<N, K>, bytes, done);
+    if (e != cudaSuccess)
+        return e;
+    const int dx = dec_cols(r);
+    const dim3 grid((unsigned)((a.w / 2 + dx - 1) / dx),
+                    (unsigned)((a.h / 2 + kDY - 1) / kDY), (unsigned)a.nframes);
+    decimate_tma_kernel<N, K><<<grid, kDecThreads, bytes, st>>>(mx, my, a, tp);
+    *used = true;
+    return cudaGetLastError();
+}
+
+} // namespace
 
 cudaError_t stats_dispatch_u8(const StatsArgs &, const Taps &, cudaStream_t);
 cudaError_t stats_dispatch_u16(const StatsArgs &, const Taps &, cudaStream_t);
@@ -17,14 +129,25 @@ cudaError_t launch_stats(const StatsArgs &a, const Taps &tp, cudaStream_t st)
     }
 }
 
+template <int N, SrcKind K>
+static cudaError_t dec_fixed_u(const DecArgs &a, const Taps &tp,
+                               cudaStream_t st)
+{
+    bool used = false;
+    const cudaError_t e = run_decimate_tma<N, K>(a, tp, st, &used);
+    if (e != cudaSuccess || used)
+        return e;
+    return run_decimate<N, K>(a, tp, st);
+}
+
 template <SrcKind K>
 static cudaError_t dec_dispatch_u(const DecArgs &a, const Taps &tp,
                                   cudaStream_t st)
 {
     switch (tp.fixed_ok ? tp.n : 0) {
-    case 5: return run_decimate<5, K>(a, tp, st);
-    case 9: return run_decimate<9, K>(a, tp, st);
-    case 19: return run_decimate<19, K>(a, tp, st);
+    case 5: return dec_fixed_u<5, K>(a, tp, st);
+    case 9: return dec_fixed_u<9, K>(a, tp, st);
+    case 19: return dec_fixed_u<19, K>(a, tp, st);
     default: return run_decimate<0, K>(a, tp, st);
     }
 }

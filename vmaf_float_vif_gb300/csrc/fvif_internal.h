@@ -90,6 +90,9 @@ struct DecArgs {
     int nframes;
     float2 *dst;
     size_t dst_frame_elems;
+    /* device word that a decimation whose staged tile did not arrive in
+     * time marks (bit 0); nullptr: that variant is not used */
+    unsigned *status = nullptr;
 };
 
 /* Final per-(frame, scale) reduction over the row sums. */
