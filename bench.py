@@ -272,8 +272,9 @@ def host_breakdown(t, wall_ms: float, nbytes: int):
     per-chunk events (fvif_profile_host): the copies' busy time and rate,
     the copy stream's idle gaps between chunks, how long chunks waited on
     a busy lane after arriving, the device span, the host's enqueue time
-    and what the call spent outside the device span."""
-    c0, c1, s0, s1, h0, h1 = (t[:, k] for k in range(6))
+    what the call spent outside the device span, and whether the library
+    saw every chunk's inputs as page-locked."""
+    c0, c1, s0, s1, h0, h1, locked = (t[:, k] for k in range(7))
     copy_ms = float(np.sum(c1 - c0))
     return {"copy_ms": round(copy_ms, 2),
             "copy_gbs": round(nbytes / (copy_ms / 1e3) / 1e9, 1),
@@ -282,7 +283,8 @@ def host_breakdown(t, wall_ms: float, nbytes: int):
             "lane_busy_after_copy_ms": round(float(np.sum(s0 - c1)), 2),
             "device_ms": round(float(np.max(s1)), 2),
             "enqueue_ms": round(float(h1[-1]), 2),
-            "outside_device_ms": round(wall_ms - float(np.max(s1)), 2)}
+            "outside_device_ms": round(wall_ms - float(np.max(s1)), 2),
+            "inputs_page_locked": bool(np.all(locked == 1.0))}
 
 
 def host_link_gbs(copies: int = 8):
@@ -333,6 +335,96 @@ def frame_ops(w: int, h: int, taps) -> int:
     return ops
 
 
+def measured_alu_peak(local_rank: int, iters: int = 800_000, reps: int = 3):
+    """The measured rate of separately rounded fp32 multiplies and adds on
+    this GPU (fvif_alu_probe: independent mul-then-add chains in every lane,
+    scalar and packed two-lane forms, about 50 ms per launch, best of
+    reps), with the SM clock sampled while it runs.  The larger of the two
+    forms is the roofline's peak."""
+    import vmaf_float_vif_gb300 as fv
+    fv.fvif_alu_probe(False, iters // 8)
+    fv.fvif_alu_probe(True, iters // 8)
+    best = {}
+    with ClockSampler(local_rank) as clk:
+        for packed in (False, True):
+            rates = []
+            for _ in range(reps):
+                ops, ms = fv.fvif_alu_probe(packed, iters)
+                rates.append(ops / (ms / 1e3) / 1e12)
+            best["packed" if packed else "scalar"] = max(rates)
+    c = clk.summary()
+    return {"tops": max(best.values()), "scalar_tops": best["scalar"],
+            "packed_tops": best["packed"], "clocks": c}
+
+
+def also_line(name, args, alu, inputs=None):
+    """Device-resident throughput of another workload (same timing as the
+    main line), with its own ALU roofline for the scale-0 statistic launch
+    and the whole step, its clocks, and the oracle on a sample of it."""
+    import torch
+    import vmaf_float_vif_gb300 as fv
+    case, (ref, dist_np) = inputs if inputs else make_inputs(name)
+    _, frames, ks = WORKLOADS[name]
+
+    def as_dev(a):
+        return torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16
+                                else a).to("cuda")
+    r, d = as_dev(ref), as_dev(dist_np)
+    out = torch.empty(4 * frames, dtype=torch.float64, device="cuda")
+    stream = torch.cuda.Stream()
+    with fv.Context(case.w, case.h, case.bitdepth, ks, case.nsq) as ctx:
+        ctx.set_stream(stream)
+        taps = [len(ctx.taps(s)) for s in range(4)]
+        chunk = ctx.chunk_frames
+        for _ in range(args.warmup):
+            ctx.score_async(r, d, out)
+        torch.cuda.synchronize()
+        ctx.profile(True)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with ClockSampler(int(os.environ.get("LOCAL_RANK", "0"))) as clocks:
+            e0.record(stream)
+            for _ in range(args.steps):
+                ctx.score_async(r, d, out)
+            e1.record(stream)
+            torch.cuda.synchronize()
+        prof = ctx.profile_read()
+        ctx.profile(False)
+    ms = e0.elapsed_time(e1) / args.steps
+    del r, d, out
+    st0_ms, st0_n = prof["stats_scale0"]
+    launches_step = -(-frames // chunk)
+    frames_launch = frames / launches_step
+    ops_launch = frames_launch * case.w * case.h * stats_ops_per_pixel(taps[0])
+    achieved = ops_launch / (st0_ms / max(1, st0_n) / 1e3) / 1e12
+    step_ops = frames * frame_ops(case.w, case.h, taps)
+    traffic = load_traffic(name, frames_launch)
+    line = {"workload": describe(name), "value": frames / (ms / 1e3),
+            "unit": "frame-pairs/s", "ms_per_step": ms,
+            "frames_per_step": frames, "chunk_frames": chunk, "taps": taps,
+            "roofline": {
+                "kernel": "stats_kernel, scale 0 (%d taps), %.4g frames per "
+                          "launch" % (taps[0], frames_launch),
+                "bound": "alu", "achieved": achieved, "peak": alu["tops"],
+                "unit": "TFLOP/s", "frac": achieved / alu["tops"],
+                "peak_note": "of measured (fvif_alu_probe)",
+                "launch_ms": st0_ms / max(1, st0_n),
+                "traffic": traffic,
+                "traffic_note": traffic_note(traffic, TRAFFIC_PATH, True),
+                "step_achieved": step_ops / (ms / 1e3) / 1e12,
+                "step_frac": step_ops / (ms / 1e3) / 1e12 / alu["tops"]},
+            "clocks": clocks.summary()}
+    if not args.no_cpu_baseline:
+        cores = host_cores()
+        rate, n, dt = oracle_rate(case, ref, dist_np, ks, cores, cores)
+        line["cpu_baseline"] = {
+            "value": rate, "unit": "frame-pairs/s", "cores": cores,
+            "kind": "oracle",
+            "sample": "%d frames of the workload, one per host thread, "
+                      "%.1f s wall" % (n, dt)}
+    return line
+
+
 def run_ours(args):
     import torch
     import vmaf_float_vif_gb300 as fv
@@ -371,6 +463,7 @@ def run_ours(args):
         for _ in range(args.warmup):
             ctx.score_async(r_dev, d_dev, out)
     torch.cuda.synchronize()
+    alu = measured_alu_peak(local_rank)
 
     ctx.profile(True)
     start = torch.cuda.Event(enable_timing=True)
@@ -414,49 +507,71 @@ def run_ours(args):
     # e2e: host buffers, copies inside the timed region
     e2e = None
     if not args.no_e2e:
-        pr = torch.from_numpy(ref.view(np.int16) if ref.dtype == np.uint16
-                              else ref).pin_memory()
-        pd = torch.from_numpy(dist_np.view(np.int16)
-                              if dist_np.dtype == np.uint16
-                              else dist_np).pin_memory()
-        hr = pr.numpy().view(ref.dtype)
-        hd = pd.numpy().view(dist_np.dtype)
+        # the inputs in page-locked buffers from the library's own host
+        # allocator (fvif_host_alloc: huge-page aligned and registered)
+        bufs = [fv.HostBuffer(ref.nbytes), fv.HostBuffer(dist_np.nbytes)]
+        hr = bufs[0].array(ref.shape, ref.dtype)
+        hd = bufs[1].array(dist_np.shape, dist_np.dtype)
+        np.copyto(hr, ref)
+        np.copyto(hd, dist_np)
+
+        def as_torch(a):
+            return torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16
+                                    else a)
+        pr, pd = as_torch(hr), as_torch(hd)
         h2d_bytes = int(ref.nbytes + dist_np.nbytes)
         link = host_link_gbs()
         control = chunked_copy_control(pr, pd, case.w * case.h)
         ctx.set_stream(None)
-        for _ in range(max(1, args.warmup)):
-            ctx.score_host(hr, hd)
-        barrier()
-        torch.cuda.synchronize()
-        # the library's per-chunk events stay on through the timed steps
-        # (a few event records per chunk); each step's table is read
-        # between steps, outside the step's own time
-        ctx.profile(True)
-        gc.collect()
-        gc.disable()
-        step_ms = []
-        parts = []
-        for _ in range(args.e2e_steps):
-            ts = time.perf_counter()
-            host_scores = ctx.score_host(hr, hd)   # returns after the d2h read
-            step_ms.append(1e3 * (time.perf_counter() - ts))
-            parts.append(host_breakdown(ctx.profile_host(), step_ms[-1],
-                                        h2d_bytes))
-        gc.enable()
-        ctx.profile(False)
-        barrier()
+
+        def e2e_run(r_host, d_host, steps):
+            """steps timed fvif_score_host calls (after warm-up), with the
+            library's per-chunk events on; each step's table is read
+            between steps, outside the step's own time."""
+            for _ in range(max(1, args.warmup)):
+                ctx.score_host(r_host, d_host)
+            barrier()
+            torch.cuda.synchronize()
+            ctx.profile(True)
+            gc.collect()
+            gc.disable()
+            times, tables = [], []
+            for _ in range(steps):
+                ts = time.perf_counter()
+                res = ctx.score_host(r_host, d_host)  # after the d2h read
+                times.append(1e3 * (time.perf_counter() - ts))
+                tables.append(host_breakdown(ctx.profile_host(), times[-1],
+                                             h2d_bytes))
+            gc.enable()
+            ctx.profile(False)
+            barrier()
+            return res, times, tables
+
+        host_scores, step_ms, parts = e2e_run(hr, hd, args.e2e_steps)
         wall = max_over_ranks(sum(step_ms) / 1e3, world)
         control_after = chunked_copy_control(pr, pd, case.w * case.h)
         link_after = host_link_gbs()
         if not np.array_equal(host_scores, scores):
             raise RuntimeError("fvif_score_host and fvif_score_async differ")
+        # the same calls from buffers pinned by torch (cudaHostAlloc), for
+        # comparison: their copy rate is what the host allocator avoids
+        tr = torch.from_numpy(ref.view(np.int16) if ref.dtype == np.uint16
+                              else ref).pin_memory()
+        td = torch.from_numpy(dist_np.view(np.int16)
+                              if dist_np.dtype == np.uint16
+                              else dist_np).pin_memory()
+        alt_scores, alt_ms, alt_parts = e2e_run(
+            tr.numpy().view(ref.dtype), td.numpy().view(dist_np.dtype),
+            args.e2e_steps)
+        if not np.array_equal(alt_scores, scores):
+            raise RuntimeError("fvif_score_host differs on torch buffers")
+        del tr, td
         e2e = {"value": job_throughput(frames, args.e2e_steps, world, wall),
                "unit": "frame-pairs/s",
                "h2d_bytes_per_step": h2d_bytes,
                "d2h_bytes_per_step": int(scores.nbytes),
                "ms_per_step": 1e3 * wall / args.e2e_steps,
-               "api": "fvif_score_host (page-locked host inputs)",
+               "api": "fvif_score_host (inputs in fvif_host_alloc buffers)",
                "step_ms": [round(t, 2) for t in step_ms],
                "median_step_ms": float(np.median(step_ms)),
                "value_at_median_step": job_throughput(
@@ -474,9 +589,16 @@ def run_ours(args):
                    "before_gbs": round(control[1], 1),
                    "after_ms": round(control_after[0], 2),
                    "after_gbs": round(control_after[1], 1),
-                   "note": "the same page-locked buffers copied in chunks "
-                           "of 16 frames with no kernels, one stream, "
-                           "median of 3 whole steps"},
+                   "note": "the same host buffers copied in chunks of 16 "
+                           "frames with no kernels, one stream, median of 3 "
+                           "whole steps"},
+               "torch_pinned": {
+                   "value": job_throughput(frames, args.e2e_steps, world,
+                                           sum(alt_ms) / 1e3),
+                   "step_ms": [round(t, 2) for t in alt_ms],
+                   "copy_gbs": [b["copy_gbs"] for b in alt_parts],
+                   "note": "the same fvif_score_host calls from buffers "
+                           "made by torch's pin_memory (cudaHostAlloc)"},
                "h2d_link_gbs": {
                    "before": [round(x, 1) for x in link],
                    "after": [round(x, 1) for x in link_after]},
@@ -487,6 +609,9 @@ def run_ours(args):
                             "after the e2e region; a step cannot finish faster "
                             "than its input bytes over the link at its "
                             "best"}
+        del pr, pd, hr, hd
+        for b in bufs:
+            b.close()
 
     if rank != 0:
         ctx.close()
@@ -519,7 +644,8 @@ def run_ours(args):
     ops_solo = n_solo * px0 * stats_ops_per_pixel(n0)
     avg_ms = st0_ms / max(1, st0_n)
     achieved = ops_launch / (avg_ms / 1e3) / 1e12
-    alu_peak = SMS * FP32_LANES_PER_SM * sm_max * 1e6 / 1e12
+    alu_derived = SMS * FP32_LANES_PER_SM * sm_max * 1e6 / 1e12
+    alu_peak = alu["tops"]
     traffic = load_traffic(args.workload, frames_launch)
     kernel_shares = {k: {"ms": v[0], "launches": v[1],
                          "share": v[0] / max(1e-9, sum(x[0] for x in
@@ -574,9 +700,15 @@ def run_ours(args):
                         "plus the products, statistic, terms and log2)"
                         % stats_ops_per_pixel(n0),
             "launch_ms": avg_ms,
-            "peak_note": "%d SMs x %d fp32 lanes x %.0f MHz, one non-fused op "
-                         "per lane per clock" % (SMS, FP32_LANES_PER_SM,
-                                                 sm_max),
+            "peak_note": "of measured: fvif_alu_probe, separately rounded "
+                         "fp32 multiply-then-add chains in every lane (best "
+                         "of scalar %.2f and packed two-lane %.2f T ops/s, "
+                         "SM clock median %s MHz while it ran); derived "
+                         "%d SMs x %d lanes x %.0f MHz = %.2f T" % (
+                             alu["scalar_tops"], alu["packed_tops"],
+                             alu["clocks"].get("sm_mhz"), SMS,
+                             FP32_LANES_PER_SM, sm_max, alu_derived),
+            "frac_of_derived": achieved / alu_derived,
             "launch_note": "events on the launching stream; consecutive chunks "
                            "run on two streams, so a launch shares the GPU "
                            "with the other chunk's smaller kernels",
@@ -597,8 +729,16 @@ def run_ours(args):
         "clocks": clk,
     }
     ctx.close()
-    if args.also and args.also != args.workload:
-        line["also"] = secondary(args.also, args)
+    also = [a for a in (args.also or "").split(",") if a and
+            a != args.workload]
+    if also:
+        line["also"] = {}
+        for name in also:
+            same = (WORKLOADS[name][0] == WORKLOADS[args.workload][0] and
+                    WORKLOADS[name][1] == frames)
+            line["also"][name] = also_line(
+                name, args, alu,
+                inputs=(case, (ref, dist_np)) if same else None)
     if not args.no_ssim:
         line["ssim_decimate"] = ssim_decimate_lines(
             args, hbm_peak, hbm_src, cpu_baseline=not args.no_cpu_baseline)
@@ -745,36 +885,6 @@ def run_ssim_only(args):
                       "warmup": max(3, args.warmup)}), flush=True)
 
 
-def secondary(name, args):
-    """Device-resident throughput of a second workload (same timing)."""
-    import torch
-    import vmaf_float_vif_gb300 as fv
-    case, (ref, dist_np) = make_inputs(name)
-    _, frames, ks = WORKLOADS[name]
-
-    def as_dev(a):
-        return torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16
-                                else a).to("cuda")
-    r, d = as_dev(ref), as_dev(dist_np)
-    out = torch.empty(4 * frames, dtype=torch.float64, device="cuda")
-    stream = torch.cuda.Stream()
-    with fv.Context(case.w, case.h, case.bitdepth, ks, case.nsq) as ctx:
-        ctx.set_stream(stream)
-        for _ in range(args.warmup):
-            ctx.score_async(r, d, out)
-        torch.cuda.synchronize()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(args.steps):
-            ctx.score_async(r, d, out)
-        e1.record(stream)
-        torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / args.steps
-    return {"workload": describe(name), "value": frames / (ms / 1e3),
-            "unit": "frame-pairs/s", "ms_per_step": ms}
-
-
 def run_reference(args):
     rank, _, world = dist_env()
     if rank != 0:
@@ -845,10 +955,18 @@ def main():
                     help="only the float_ssim decimation measurement (one "
                          "JSON line; the small case the decimation profiles "
                          "are captured on)")
-    ap.add_argument("--also", choices=sorted(WORKLOADS) + [""],
-                    default="c2_1080p_10b",
-                    help="second workload timed device-resident (\"\" = none)")
+    ap.add_argument("--also",
+                    default=",".join(w for w in WORKLOADS
+                                     if w != "c5_4k_10b"),
+                    help="comma-separated other workloads timed "
+                         "device-resident, each with its own roofline and "
+                         "oracle baseline (\"\" = none; default: every "
+                         "other workload)")
     args = ap.parse_args()
+    for name in (args.also or "").split(","):
+        if name and name not in WORKLOADS:
+            ap.error("--also: unknown workload %r (choose from %s)" %
+                     (name, ", ".join(sorted(WORKLOADS))))
     if args.warmup < 3 and args.impl == "ours":
         print("note: fewer than 3 warm-up steps", file=sys.stderr)
     if args.impl == "reference":

@@ -56,6 +56,11 @@
  *    second makes its CTA give up and the next synchronous call on the
  *    context (fvif_score, fvif_score_host, fvif_score_debug) return
  *    FVIF_ECUDA.
+ *  - FVIF_TEST_DEC_STALL=1: test hook, read by fvif_create: the staged
+ *    decimation of that context waits for 16 bytes more than its tensor
+ *    copies deliver, so every such wait runs into its one-second limit and
+ *    the synchronous calls return FVIF_ECUDA (the timeout path, exercised
+ *    without any fault).
  *  - FVIF_FAIL_ALLOC=n: test hook, read by fvif_create: allocation n
  *    (0 = the first) of the context fails as if the device were out of
  *    memory, so every failure path can be exercised without exhausting
@@ -63,6 +68,8 @@
  */
 #ifndef FVIF_H
 #define FVIF_H
+
+#include <stddef.h>
 
 #ifdef __cplusplus
 extern "C" {
@@ -148,6 +155,20 @@ int fvif_score_async(fvif_ctx *ctx, const void *ref, const void *dist,
  * work, slower).  out: HOST memory of 4*n_frames doubles.  Synchronous. */
 int fvif_score_host(fvif_ctx *ctx, const void *ref, const void *dist,
                     int n_frames, double *out);
+
+/* Page-locked HOST memory for the inputs of fvif_score_host: bytes rounded
+ * up to the transparent-huge-page size (at least 2 MiB), aligned to it,
+ * advised for huge pages and registered with the CUDA driver
+ * (cudaHostRegister) on behalf of every device.  The copy engine moved
+ * such buffers at the host link's full rate where large cudaHostAlloc
+ * buffers varied by up to 9x.  The pages have no counterpart: this is a
+ * host-memory helper of the library's input path.  Returns NULL if
+ * bytes == 0 or on failure.  Free with fvif_host_free only. */
+void *fvif_host_alloc(size_t bytes);
+
+/* Release a buffer from fvif_host_alloc; NULL and unknown pointers are
+ * ignored.  No call may still be using it. */
+void fvif_host_free(void *p);
 
 /* As fvif_score, with the fifteen debug outputs per frame in HOST memory
  * (out: 15*n_frames doubles, frame-major): vif_scale0..3, the frame ratio

@@ -8,6 +8,8 @@
 - A destroyed context is rejected, not dereferenced; destroying it twice is
   a no-op.
 """
+import ctypes
+
 import numpy as np
 import pytest
 
@@ -138,3 +140,35 @@ def test_use_after_destroy_is_rejected(fv):
     ctx2 = L.fvif_create(96, 64, 10, 1.0, 2.0)
     assert ctx2
     L.fvif_destroy(ctx2)
+
+
+def test_staged_decimation_wait_times_out_cleanly(fv, monkeypatch):
+    """The staged first decimation's mbarrier wait is bounded: with the
+    test hook its phase can never complete (16 bytes more expected than the
+    tensor copies deliver), every CTA gives up after one second, marks the
+    context's status word and returns; fvif_score reports FVIF_ECUDA, the
+    GPU stays usable and a context without the hook scores correctly."""
+    import time
+    import torch
+    case = S.custom_noise_case(192, 140, 10, frames=2, seed=5)
+    ref, dist = case.batch(range(2))
+    r = torch.from_numpy(ref.view(np.int16)).cuda()
+    d = torch.from_numpy(dist.view(np.int16)).cuda()
+    L = fv.lib()
+    monkeypatch.setenv("FVIF_TEST_DEC_STALL", "1")
+    ctx = L.fvif_create(case.w, case.h, 10, 1.0, 2.0)
+    monkeypatch.delenv("FVIF_TEST_DEC_STALL")
+    assert ctx
+    out = np.zeros(8, np.float64)
+    t0 = time.perf_counter()
+    st = L.fvif_score(ctx, r.data_ptr(), d.data_ptr(), 2,
+                      out.ctypes.data_as(ctypes.c_void_p))
+    dt = time.perf_counter() - t0
+    L.fvif_destroy(ctx)
+    assert st == fv.FVIF_ECUDA, st
+    assert 0.9 < dt < 30.0, dt
+    torch.cuda.synchronize()
+    want = oracle.score(ref, dist, 10, 1.0, 2.0)
+    with fv.Context(case.w, case.h, 10, 1.0, 2.0) as good:
+        got = good.score(r, d)
+    assert np.array_equal(got.view(np.uint64), want.view(np.uint64))

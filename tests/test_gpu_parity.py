@@ -319,6 +319,33 @@ def test_host_path_chunk_timing(fv):
     assert np.all(h1 >= h0) and np.all(h0[1:] >= h1[:-1])
 
 
+def test_host_alloc_buffers(fv):
+    """Frames staged in fvif_host_alloc buffers score like any host input,
+    the library sees them as page-locked, a ragged tail of frames fits, and
+    freeing twice or freeing an unknown pointer does nothing."""
+    case = S.custom_noise_case(320, 180, 10, frames=19)
+    ref, dist = case.batch(range(case.frames))
+    want = oracle_scores(ref, dist, 10, 1.0, 2.0)
+    br, bd = fv.HostBuffer(ref.nbytes), fv.HostBuffer(dist.nbytes)
+    hr, hd = br.array(ref.shape, ref.dtype), bd.array(dist.shape, dist.dtype)
+    np.copyto(hr, ref)
+    np.copyto(hd, dist)
+    with fv.Context(case.w, case.h, 10, 1.0, 2.0) as ctx:
+        ctx.profile(True)
+        assert_bitwise(ctx.score_host(hr, hd), want, "host_alloc buffers")
+        t = ctx.profile_host()
+        ctx.profile(False)
+    assert np.all(t[:, 6] == 1.0)
+    del hr, hd
+    L = fv.lib()
+    p = br.ptr
+    br.close()
+    br.close()
+    L.fvif_host_free(p)       # already freed: ignored
+    bd.close()
+    assert L.fvif_host_alloc(0) is None
+
+
 def test_zero_frames_and_bad_calls(fv):
     torch = torch_mod()
     with fv.Context(64, 48, 8, 1.0, 2.0) as ctx:

@@ -231,3 +231,16 @@ def test_every_environment_variable_is_documented():
             headers += f.read()
     assert read, "no getenv call found"
     assert not [v for v in read if v not in headers], read
+
+
+def test_host_alloc_degenerate_calls_need_no_gpu():
+    """fvif_host_alloc(0) returns NULL and fvif_host_free ignores NULL and
+    pointers it did not make, without touching CUDA."""
+    import ctypes
+    from vmaf_float_vif_gb300 import _lib
+    _lib.build()
+    L = _lib.lib()
+    assert L.fvif_host_alloc(0) is None
+    L.fvif_host_free(None)
+    junk = ctypes.create_string_buffer(64)
+    L.fvif_host_free(ctypes.addressof(junk))

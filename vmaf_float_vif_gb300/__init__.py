@@ -17,6 +17,7 @@ from ._lib import (  # noqa: F401
     fvif_get_taps, fvif_last_error, fvif_score, fvif_score_async,
     fvif_score_host, fvif_set_stream, fvif_strerror, fvif_profile_enable,
     fvif_profile_read, fvif_profile_host, HOST_PROFILE_COLUMNS,
+    fvif_alu_probe, HostBuffer,
     fvif_debug_terms, fvif_create_ex, fvif_score_debug,
     fvif_default_options, FvifOptions, KERNEL_KINDS, Context, plane_sizes,
     fssim_auto_scale, fssim_decimated_size, fssim_decimate)

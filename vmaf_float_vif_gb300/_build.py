@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(OUT_DIR, "libfvif.so")
 
 SOURCES = ["fvif_api.cu", "fvif_stats_u8.cu", "fvif_stats_u16.cu",
            "fvif_stats_f2.cu", "fvif_decimate.cu", "fvif_noalloc.cu",
-           "fvif_probe.cu",
+           "fvif_probe.cu", "fvif_hostmem.cu",
            "fssim_api.cu", "fssim_u8.cu", "fssim_u16.cu"]
 HEADERS = ["fvif_internal.h", "fvif_kernels.cuh", "fvif_dispatch.cuh",
            "fvif_dec_tma.cuh",

@@ -28,6 +28,7 @@ EXPORTS = (
     "fvif_destroy", "fvif_set_stream", "fvif_last_error", "fvif_strerror",
     "fvif_chunk_frames", "fvif_get_taps", "fvif_debug_frame",
     "fvif_profile_enable", "fvif_profile_read", "fvif_profile_host",
+    "fvif_alu_probe", "fvif_host_alloc", "fvif_host_free",
     "fvif_score_noalloc",
     "fvif_debug_terms", "fvif_default_options", "fvif_create_ex",
     "fvif_score_debug",
@@ -99,6 +100,12 @@ def _declare(L: ctypes.CDLL) -> ctypes.CDLL:
     L.fvif_profile_enable.restype = i
     L.fvif_profile_read.argtypes = [vp, i, dp, ctypes.POINTER(ctypes.c_longlong)]
     L.fvif_profile_read.restype = i
+    L.fvif_host_alloc.argtypes = [ctypes.c_size_t]
+    L.fvif_host_alloc.restype = vp
+    L.fvif_host_free.argtypes = [vp]
+    L.fvif_host_free.restype = None
+    L.fvif_alu_probe.argtypes = [i, ctypes.c_longlong, vp, dp, dp]
+    L.fvif_alu_probe.restype = i
     L.fvif_profile_host.argtypes = [vp, dp, i]
     L.fvif_profile_host.restype = i
     L.fvif_default_options.argtypes = [ctypes.POINTER(FvifOptions)]
@@ -400,18 +407,66 @@ def fvif_profile_read(ctx: int, kind: int):
     return ms.value, n.value
 
 
+class HostBuffer:
+    """Page-locked host memory from fvif_host_alloc (freed by close() or
+    when the object is collected; arrays made by ``array`` must not be used
+    after that)."""
+
+    def __init__(self, nbytes: int):
+        self.nbytes = int(nbytes)
+        self.ptr = lib().fvif_host_alloc(self.nbytes)
+        if not self.ptr:
+            raise MemoryError("fvif_host_alloc(%d) failed" % self.nbytes)
+
+    def array(self, shape, dtype) -> np.ndarray:
+        """A numpy array over the start of the buffer."""
+        dt = np.dtype(dtype)
+        n = int(np.prod(shape)) * dt.itemsize
+        if n > self.nbytes:
+            raise ValueError("buffer holds %d bytes, %d wanted" %
+                             (self.nbytes, n))
+        raw = (ctypes.c_uint8 * n).from_address(self.ptr)
+        return np.frombuffer(raw, dtype=dt).reshape(shape)
+
+    def close(self) -> None:
+        if self.ptr:
+            lib().fvif_host_free(self.ptr)
+            self.ptr = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def fvif_alu_probe(packed: bool, iters: int, stream=None):
+    """(operations, ms) of one probe launch of separately rounded fp32
+    multiplies and adds (scalar or packed two-lane forms)."""
+    ops = ctypes.c_double()
+    ms = ctypes.c_double()
+    handle = getattr(stream, "cuda_stream", stream)
+    st = lib().fvif_alu_probe(1 if packed else 0, int(iters), handle or None,
+                              ctypes.byref(ops), ctypes.byref(ms))
+    if st:
+        raise FvifError(st, "fvif_alu_probe")
+    return ops.value, ms.value
+
+
 HOST_PROFILE_COLUMNS = ("copy_start", "copy_end", "score_start",
-                        "score_end", "enqueue_start", "enqueue_end")
+                        "score_end", "enqueue_start", "enqueue_end",
+                        "page_locked")
 
 
 def fvif_profile_host(ctx: int) -> np.ndarray:
     """Per-chunk timing of the last fvif_score_host call made while
-    profiling: an (n, 6) array with the columns HOST_PROFILE_COLUMNS (device
-    ms since chunk 0's copy start, then host ms since the call began)."""
+    profiling: an (n, 7) array with the columns HOST_PROFILE_COLUMNS (device
+    ms since chunk 0's copy start, host ms since the call began, and 1 where
+    the chunk's inputs were page-locked)."""
     n = lib().fvif_profile_host(ctx, None, 0)
     if n < 0:
         raise FvifError(n, "fvif_profile_host")
-    out = np.zeros((n, 6), np.float64)
+    out = np.zeros((n, 7), np.float64)
     if n:
         got = lib().fvif_profile_host(
             ctx, out.ctypes.data_as(ctypes.POINTER(ctypes.c_double)), n)

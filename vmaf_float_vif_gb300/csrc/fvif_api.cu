@@ -175,6 +175,9 @@ struct fvif_ctx {
      * (0 = the first) fails as if the device were out of memory */
     int fail_alloc_at = -1;
     int allocs = 0;
+    /* test hook (FVIF_TEST_DEC_STALL=1): the staged decimation's waits of
+     * this context never complete, so each CTA gives up after its limit */
+    unsigned dec_extra_tx = 0;
     int device = 0;
     cudaStream_t stream = nullptr;
     int last_status = FVIF_OK;
@@ -443,6 +446,7 @@ int run_chunk(fvif_ctx *c, fvif_ctx::Lane &l, const void *ref,
         d.dst = l.pyr[s];
         d.dst_frame_elems = (size_t)c->ws[s] * c->hs[s];
         d.status = c->d_status;
+        d.extra_tx = c->dec_extra_tx;
         e = prof_begin(c, FVIF_K_DECIMATE, st);
         if (e == cudaSuccess)
             e = launch_decimate(d, c->taps[s], st);
@@ -794,6 +798,8 @@ static fvif_ctx *create_ex_impl(int w, int h, int bitdepth, float kernelscale,
         if (v >= 2 && v <= kMaxStage)
             c->stage_slots = v;
     }
+    if (const char *env = std::getenv("FVIF_TEST_DEC_STALL"))
+        c->dec_extra_tx = std::atoi(env) != 0 ? 16u : 0u;
     if (const char *env = std::getenv("FVIF_HOST_LANES")) {
         const int v = std::atoi(env);
         if (v >= 1 && v <= kLanes)

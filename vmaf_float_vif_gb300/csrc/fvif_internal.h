@@ -93,6 +93,9 @@ struct DecArgs {
     /* device word that a decimation whose staged tile did not arrive in
      * time marks (bit 0); nullptr: that variant is not used */
     unsigned *status = nullptr;
+    /* test hook: bytes the staged decimation's mbarrier expects beyond what
+     * its tensor copies deliver (0; nonzero makes every wait time out) */
+    unsigned extra_tx = 0;
 };
 
 /* Final per-(frame, scale) reduction over the row sums. */
