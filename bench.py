@@ -228,11 +228,11 @@ def load_traffic(workload, frames_per_launch):
         return None
     if t.get("kernel_hash") != kernel_hash():
         return None
-    b = t.get("per_launch_bytes", {}).get(workload)
-    n = t.get("frames_per_launch")
-    if b is None or not n:
+    cap = t.get("captures", {}).get(workload)
+    if not cap or not cap.get("frames"):
         return None
-    return b * frames_per_launch / n
+    return ((cap["dram_bytes_read"] + cap["dram_bytes_write"]) *
+            frames_per_launch / cap["frames"])
 
 
 def chunked_copy_control(pr, pd, frame_elems: int, chunk: int = 16,

@@ -52,12 +52,17 @@ def test_source_hash_ignores_comments_not_code(tmp_path, monkeypatch):
 
 def test_traffic_scales_with_frames_and_needs_the_same_kernels(
         tmp_path, monkeypatch):
-    rec = {"kernel_hash": bench.kernel_hash(), "frames_per_launch": 16,
-           "per_launch_bytes": {"c5_4k_10b": 1600}}
+    rec = {"kernel_hash": bench.kernel_hash(),
+           "captures": {"c5_4k_10b": {"frames": 16, "dram_bytes_read": 1500,
+                                      "dram_bytes_write": 100},
+                        "c1_576x324_8b": {"frames": 64,
+                                          "dram_bytes_read": 640,
+                                          "dram_bytes_write": 0}}}
     p = tmp_path / "traffic.json"
     p.write_text(json.dumps(rec))
     monkeypatch.setattr(bench, "TRAFFIC_PATH", str(p))
     assert bench.load_traffic("c5_4k_10b", 30) == 3000
+    assert bench.load_traffic("c1_576x324_8b", 192) == 1920
     assert bench.load_traffic("c4_4k_8b", 30) is None
     rec["kernel_hash"] = "0" * 16
     p.write_text(json.dumps(rec))

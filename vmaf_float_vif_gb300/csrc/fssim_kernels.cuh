@@ -57,13 +57,6 @@
 
 #include <cuda_runtime.h>
 
-/* Packed two-lane operations written with the compiler's own float2
- * intrinsics (1) instead of inline PTX (0); each lane rounds the same way
- * either way. */
-#ifndef FSSIM_PACKED_NATIVE
-#define FSSIM_PACKED_NATIVE 0
-#endif
-
 namespace fssim {
 
 constexpr int kThreads = 256;
@@ -113,9 +106,6 @@ __device__ __forceinline__ int skew(int c) { return c + (c >> 5); }
  * arguments, so the code generator cannot merge a product into them. */
 __device__ __forceinline__ float2 mul2_rn(float2 a, float2 b)
 {
-#if FSSIM_PACKED_NATIVE
-    return __fmul2_rn(a, b);
-#else
     float2 r;
     asm("{\n\t.reg .b64 pa, pb, pd;\n\t"
         "mov.b64 pa, {%2, %3};\n\t"
@@ -125,14 +115,10 @@ __device__ __forceinline__ float2 mul2_rn(float2 a, float2 b)
         : "=f"(r.x), "=f"(r.y)
         : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
     return r;
-#endif
 }
 
 __device__ __forceinline__ float2 fma2_rn(float2 a, float2 b, float2 c)
 {
-#if FSSIM_PACKED_NATIVE
-    return __ffma2_rn(a, b, c);
-#else
     float2 r;
     asm("{\n\t.reg .b64 pa, pb, pc, pd;\n\t"
         "mov.b64 pa, {%2, %3};\n\t"
@@ -143,7 +129,6 @@ __device__ __forceinline__ float2 fma2_rn(float2 a, float2 b, float2 c)
         : "=f"(r.x), "=f"(r.y)
         : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
     return r;
-#endif
 }
 
 /* Constants of the inexact-tap arithmetic, passed as launch arguments. */
