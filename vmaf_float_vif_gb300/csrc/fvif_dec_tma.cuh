@@ -259,264 +259,3 @@ __global__ void __launch_bounds__(kDecThreads)
 
 } // namespace fvif
 
-namespace fvif {
-
-/* ---------------------------------------------------------------------- */
-/* Second layout of the staged first decimation: fewer shared-memory loads
- * per output, same arithmetic in the same order.
- *  - Edge tiles first overwrite their out-of-plane samples with the
- *    samples the reflect-then-clamp boundary selects (always in-plane
- *    entries of the same tile), so every later read is a plain index.
- *  - Vertical pass: one thread per pair of adjacent tile columns and group
- *    of kD2RV output rows; one 32-bit (16-bit samples) or 16-bit (8-bit
- *    samples) load per plane and row gives both columns.
- *  - Horizontal pass: one thread per kD2H adjacent outputs of a row, reading
- *    the vertically filtered row as 16-byte pairs of float2.              */
-constexpr int kD2RV = 8; /* output rows per vertical item                  */
-#ifndef FVIF_DEC2_H
-#define FVIF_DEC2_H 4
-#endif
-constexpr int kD2H = FVIF_DEC2_H; /* outputs per horizontal item           */
-/* float2 per Vd row: at least the 128 filtered columns plus what the last
- * horizontal item reads, and 2 * pitch = 4 (mod 32) words, so that a warp
- * reading one 16-byte pair from each of 32 rows uses every bank once */
-constexpr int kD2Pitch = 146;
-static_assert((2 * kD2Pitch) % 32 == 4, "Vd row pitch and banks");
-static_assert(kDY % kD2RV == 0, "vertical groups");
-
-__host__ __device__ constexpr size_t dtma2_main_bytes(int r, int eb)
-{
-    return 2 * ((dtma_tile_bytes(r, eb) + 127) / 128 * 128) >
-                   sizeof(float2) * kDY * (size_t)kD2Pitch
-               ? 2 * ((dtma_tile_bytes(r, eb) + 127) / 128 * 128)
-               : sizeof(float2) * kDY * (size_t)kD2Pitch;
-}
-__host__ __device__ constexpr size_t dtma2_smem_bytes(int r, int eb)
-{
-    return dtma2_main_bytes(r, eb) + sizeof(uint64_t);
-}
-
-/* two samples of a pair load as (ref, dist) pairs of exact fp32 values:
- * 2^23 + s has the bits 0x4B000000 | s, and subtracting 2^23 is exact */
-template <typename T>
-__device__ __forceinline__ void dtma2_unpack(uint32_t qx, uint32_t qy,
-                                             float2 &c0, float2 &c1)
-{
-    constexpr uint32_t kMagic = 0x4B000000u;
-    uint32_t x0, x1, y0, y1;
-    if constexpr (sizeof(T) == 2) {
-        x0 = __byte_perm(qx, kMagic, 0x7610);
-        x1 = __byte_perm(qx, kMagic, 0x7632);
-        y0 = __byte_perm(qy, kMagic, 0x7610);
-        y1 = __byte_perm(qy, kMagic, 0x7632);
-    } else {
-        x0 = __byte_perm(qx, kMagic, 0x7440);
-        x1 = __byte_perm(qx, kMagic, 0x7441);
-        y0 = __byte_perm(qy, kMagic, 0x7440);
-        y1 = __byte_perm(qy, kMagic, 0x7441);
-    }
-    c0 = make_float2(__fsub_rn(__uint_as_float(x0), 8388608.0f),
-                     __fsub_rn(__uint_as_float(y0), 8388608.0f));
-    c1 = make_float2(__fsub_rn(__uint_as_float(x1), 8388608.0f),
-                     __fsub_rn(__uint_as_float(y1), 8388608.0f));
-}
-
-/* Horizontal pass of the second layout: kD2H outputs per item; OFF is the
- * Vd column of output column 0's first tap (0 or 1, the same for a whole
- * tile). */
-template <int N, int DX, int kHI, int kPairs, int OFF>
-__device__ __forceinline__ void dtma2_hpass(const float2 *Vd,
-                                            const DecArgs &a, const Taps &tp,
-                                            int x0, int y0, int f, int W2,
-                                            int H2)
-{
-    float2 *dst = a.dst + (size_t)f * a.dst_frame_elems;
-    /* a warp takes one column offset in all kDY rows (banks, see kD2Pitch) */
-    for (int it = threadIdx.x; it < kDY * kHI; it += kDecThreads) {
-        const int xl = (it / kDY) * kD2H, yl = it % kDY;
-        const int yd = y0 + yl;
-        if (yd >= H2)
-            continue;
-        const float2 *row = Vd + yl * kD2Pitch + 2 * xl;
-        float2 col[2 * kPairs];
-#pragma unroll
-        for (int u = 0; u < kPairs; ++u) {
-            const float4 v = *reinterpret_cast<const float4 *>(row + 2 * u);
-            col[2 * u] = make_float2(v.x, v.y);
-            col[2 * u + 1] = make_float2(v.z, v.w);
-        }
-#pragma unroll
-        for (int o = 0; o < kD2H; ++o) {
-            const int xd = x0 + xl + o;
-            if (xl + o >= DX || xd >= W2)
-                break;
-            float2 sum;
-#pragma unroll
-            for (int k = 0; k < N; ++k) {
-                const float2 p = mul2_rn(tp.t2[k], col[2 * o + k + OFF]);
-                sum = (k == 0) ? p : acc2_rn(sum, p, tp.one2);
-            }
-            dst[(size_t)yd * W2 + xd] = sum;
-        }
-    }
-}
-
-/* CTAs per SM the second layout's registers must allow (fixed widths up
- * to 9 taps; wider kernels take what they need) */
-#ifndef FVIF_DEC2_MINB
-#define FVIF_DEC2_MINB 4
-#endif
-template <int N, SrcKind K>
-__global__ void __launch_bounds__(kDecThreads, N <= 9 ? FVIF_DEC2_MINB : 1)
-    decimate_tma2_kernel(const __grid_constant__ CUtensorMap tmx,
-                         const __grid_constant__ CUtensorMap tmy,
-                         const DecArgs a, const Taps tp)
-{
-    using T = typename std::conditional<K == SrcKind::U8, uint8_t,
-                                        uint16_t>::type;
-    using P = typename std::conditional<K == SrcKind::U8, uint16_t,
-                                        uint32_t>::type; /* a column pair */
-    constexpr bool kRaw = K == SrcKind::U16;
-    constexpr int EB = sizeof(T);
-    constexpr int R = N / 2;
-    constexpr int DX = dec_cols(R);
-    constexpr int DW = dec_width(R);
-    constexpr int BW = dtma_bw(R, EB);
-    constexpr int BH = dtma_bh(R);
-    constexpr uint32_t kTileBytes = (uint32_t)dtma_tile_bytes(R, EB);
-    constexpr size_t kTileStride = (dtma_tile_bytes(R, EB) + 127) / 128 * 128;
-    constexpr int NP = 64; /* column pairs per tile row that are filtered */
-    static_assert(N > 0 && N <= kMaxFixedTaps, "fixed widths only");
-    static_assert((BW * EB) % 16 == 0 && BW <= 256 && BH <= 256,
-                  "tensor-copy box");
-    static_assert(DW <= 2 * NP - 1 && 2 * NP + 1 <= BW + 1, "pair range");
-    static_assert(NP * (kDY / kD2RV) == kDecThreads,
-                  "one vertical item per thread");
-    static_assert(2 * NP + 3 <= kD2Pitch, "Vd row");
-
-    extern __shared__ __align__(16) unsigned char smem_raw[];
-    T *tx = reinterpret_cast<T *>(smem_raw);
-    T *ty = reinterpret_cast<T *>(smem_raw + kTileStride);
-    float2 *Vd = reinterpret_cast<float2 *>(smem_raw);
-    uint64_t &bar =
-        *reinterpret_cast<uint64_t *>(smem_raw + dtma2_main_bytes(R, EB));
-
-    const int W = a.w, H = a.h, W2 = W / 2, H2 = H / 2;
-    const int x0 = blockIdx.x * DX, y0 = blockIdx.y * kDY, f = blockIdx.z;
-    const int p0 = 2 * x0 - R;
-    const int xs = p0 & ~(dtma_align(EB) - 1); /* floor, also below 0 */
-    const int ys = 2 * y0 - R;
-    const int q0 = (p0 - xs) >> 1; /* first column pair the tile filters */
-    const int c0 = (p0 - xs) & 1;  /* Vd column of output column 0's tap 0 */
-
-    if (threadIdx.x == 0) {
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(
-                         smem_addr(&bar))
-                     : "memory");
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        asm volatile(
-            "mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(
-                smem_addr(&bar)),
-            "r"(2 * kTileBytes + a.extra_tx)
-            : "memory");
-        asm volatile("cp.async.bulk.tensor.3d.shared::cluster.global.tile"
-                     ".mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}],"
-                     " [%5];" ::"r"(smem_addr(tx)),
-                     "l"(reinterpret_cast<uint64_t>(&tmx)), "r"(xs), "r"(ys),
-                     "r"(f), "r"(smem_addr(&bar))
-                     : "memory");
-        asm volatile("cp.async.bulk.tensor.3d.shared::cluster.global.tile"
-                     ".mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}],"
-                     " [%5];" ::"r"(smem_addr(ty)),
-                     "l"(reinterpret_cast<uint64_t>(&tmy)), "r"(xs), "r"(ys),
-                     "r"(f), "r"(smem_addr(&bar))
-                     : "memory");
-    }
-    bool arrived = mbar_try_wait(&bar, 0);
-    if (!arrived) {
-        const uint64_t t0 = global_ns();
-        while (!(arrived = mbar_try_wait(&bar, 0)) &&
-               global_ns() - t0 < 1000000000ull) {
-        }
-    }
-    if (__syncthreads_or(!arrived)) {
-        if (threadIdx.x == 0 && a.status)
-            atomicOr(a.status, 1u);
-        return;
-    }
-
-    /* edge tiles: out-of-plane entries take the entry the boundary rule
-     * selects, clamped into the tile's in-plane part (entries only unused
-     * outputs would read); in-plane entries are never written, so the
-     * copies do not depend on one another */
-    if (xs < 0 || ys < 0 || xs + BW > W || ys + BH > H) {
-        const int clo = max(0, -xs), chi = min(BW, W - xs) - 1;
-        const int rlo = max(0, -ys), rhi = min(BH, H - ys) - 1;
-        for (int e = threadIdx.x; e < BW * BH; e += kDecThreads) {
-            const int r = e / BW, c = e - r * BW;
-            const bool rin = r >= rlo && r <= rhi, cin = c >= clo && c <= chi;
-            if (rin && cin)
-                continue;
-            const int sr = min(max(bound_index(ys + r, H) - ys, rlo), rhi);
-            const int sc = min(max(bound_index(xs + c, W) - xs, clo), chi);
-            tx[e] = tx[sr * BW + sc];
-            ty[e] = ty[sr * BW + sc];
-        }
-        __syncthreads();
-    }
-
-    /* vertical pass: pair q (tile columns 2(q0+q), +1), rows 2*kD2RV*g .. */
-    const int q = threadIdx.x % NP;
-    const int g = threadIdx.x / NP;
-    float2 acc0[kD2RV], acc1[kD2RV];
-    {
-        const P *px = reinterpret_cast<const P *>(tx) + q0 + q;
-        const P *py = reinterpret_cast<const P *>(ty) + q0 + q;
-        int idx = (2 * kD2RV * g) * (BW / 2);
-#pragma unroll
-        for (int t = 0; t < 2 * (kD2RV - 1) + N; ++t) {
-            float2 v0, v1;
-            dtma2_unpack<T>((uint32_t)px[idx], (uint32_t)py[idx], v0, v1);
-            idx += BW / 2;
-#pragma unroll
-            for (int i = 0; i < kD2RV; ++i) {
-                const int k = t - 2 * i;
-                if (k >= 0 && k < N) {
-                    const int kk = fold(k, N);
-                    const float2 tk = kRaw ? tp.ra2[kk] : tp.t2[kk];
-                    const float2 m0 = mul2_rn(tk, v0);
-                    const float2 m1 = mul2_rn(tk, v1);
-                    acc0[i] = (k == 0) ? m0 : acc2_rn(acc0[i], m0, tp.one2);
-                    acc1[i] = (k == 0) ? m1 : acc2_rn(acc1[i], m1, tp.one2);
-                }
-            }
-        }
-    }
-    __syncthreads(); /* the tiles are read; Vd reuses their memory */
-#pragma unroll
-    for (int i = 0; i < kD2RV; ++i)
-        *reinterpret_cast<float4 *>(Vd + (g * kD2RV + i) * kD2Pitch + 2 * q) =
-            make_float4(acc0[i].x, acc0[i].y, acc1[i].x, acc1[i].y);
-    __syncthreads();
-
-    /* horizontal pass: outputs xl .. xl + kD2H - 1 of row yl need Vd
-     * columns c0 + 2 xl .. c0 + 2 xl + 2 kD2H + N - 3, read as float4
-     * pairs from the even column at or below the first */
-    constexpr int kHI = (DX + kD2H - 1) / kD2H; /* items per row */
-    constexpr int kNeed = 2 * kD2H + N - 2;     /* columns an item uses */
-    /* float4 loads from the even column at or below the first one: the
-     * first column may be odd, so kNeed + 1 columns are covered */
-    constexpr int kPairs = (kNeed + 2) / 2;
-    static_assert(2 * kD2H * (kHI - 1) + 2 * kPairs <= kD2Pitch,
-                  "horizontal reads stay inside a Vd row");
-    if (c0)
-        dtma2_hpass<N, DX, kHI, kPairs, 1>(Vd, a, tp, x0, y0, f, W2, H2);
-    else
-        dtma2_hpass<N, DX, kHI, kPairs, 0>(Vd, a, tp, x0, y0, f, W2, H2);
-}
-
-} // namespace fvif

@@ -9,13 +9,6 @@
 #include "fvif_dec_tma.cuh"
 #include "fvif_dispatch.cuh"
 
-/* Which staged decimation layout the first decimation uses: 1 = one
- * column per thread with reflected reads, 2 = padded edge tiles, column
- * pairs and four outputs per horizontal item. */
-#ifndef FVIF_DEC_TMA_LAYOUT
-#define FVIF_DEC_TMA_LAYOUT 1
-#endif
-
 namespace fvif {
 
 namespace {
@@ -112,20 +105,11 @@ cudaError_t run_decimate_tma(const DecArgs &a, const Taps &tp,
     const int dx = dec_cols(r);
     const dim3 grid((unsigned)((a.w / 2 + dx - 1) / dx),
                     (unsigned)((a.h / 2 + kDY - 1) / kDY), (unsigned)a.nframes);
-#if FVIF_DEC_TMA_LAYOUT == 1
     const size_t bytes = dtma_smem_bytes(r, eb);
     cudaError_t e = ensure_smem(decimate_tma_kernel<N, K>, bytes, done);
     if (e != cudaSuccess)
         return e;
     decimate_tma_kernel<N, K><<<grid, kDecThreads, bytes, st>>>(mx, my, a, tp);
-#else
-    const size_t bytes = dtma2_smem_bytes(r, eb);
-    cudaError_t e = ensure_smem(decimate_tma2_kernel<N, K>, bytes, done);
-    if (e != cudaSuccess)
-        return e;
-    decimate_tma2_kernel<N, K><<<grid, kDecThreads, bytes, st>>>(mx, my, a,
-                                                                 tp);
-#endif
     *used = true;
     return cudaGetLastError();
 }
