@@ -720,23 +720,38 @@ ssim_decimate_windows_kernel(const DecimateParams p)
             }
             float *orow = dst + (size_t)(y0 + r) * p.sw + WT * g;
             const int nout = min(WT, p.sw - WT * g);
+            float o[WT];
 #pragma unroll
             for (int i = 0; i < WT; ++i) {
-                if (i < nout) {
-                    const unsigned Sw = i == 0 ? S[0] + Sp : S[i];
-                    float o;
-                    if constexpr (kExact) {
-                        o = __fmul_rn(__uint2float_rn(Sw), p.out_scale);
-                    } else {
-                        const float Ew = i == 0 ? __fadd_rn(E[0], Ep) : E[i];
-                        const long long n =
-                            p.T * (long long)Sw -
-                            (long long)__float2int_rn(
-                                __fmul_rn(Ew, p.err_scale));
-                        o = __fmul_rn(__ll2float_rn(n), p.out_scale);
-                    }
-                    orow[i] = o;
+                const unsigned Sw = i == 0 ? S[0] + Sp : S[i];
+                if constexpr (kExact) {
+                    o[i] = __fmul_rn(__uint2float_rn(Sw), p.out_scale);
+                } else {
+                    const float Ew = i == 0 ? __fadd_rn(E[0], Ep) : E[i];
+                    const long long n =
+                        p.T * (long long)Sw -
+                        (long long)__float2int_rn(__fmul_rn(Ew, p.err_scale));
+                    o[i] = __fmul_rn(__ll2float_rn(n), p.out_scale);
                 }
+            }
+            /* a thread's outputs are consecutive: whole chunks go out as
+             * 16- or 8-byte stores where the row start allows it */
+            const uintptr_t oa = reinterpret_cast<uintptr_t>(orow);
+            if (nout == WT && oa % 16 == 0) {
+#pragma unroll
+                for (int i = 0; i < WT; i += 4)
+                    *reinterpret_cast<float4 *>(orow + i) =
+                        make_float4(o[i], o[i + 1], o[i + 2], o[i + 3]);
+            } else if (nout == WT && oa % 8 == 0) {
+#pragma unroll
+                for (int i = 0; i < WT; i += 2)
+                    *reinterpret_cast<float2 *>(orow + i) =
+                        make_float2(o[i], o[i + 1]);
+            } else {
+#pragma unroll
+                for (int i = 0; i < WT; ++i)
+                    if (i < nout)
+                        orow[i] = o[i];
             }
         }
     }
