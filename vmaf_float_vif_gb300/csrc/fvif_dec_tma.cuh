@@ -56,12 +56,17 @@ __host__ __device__ constexpr size_t dtma_tile_bytes(int r, int eb)
 /* dynamic shared memory: the two sample tiles (128-byte aligned), reused
  * for the vertically filtered rows Vd once the tiles have been read, then
  * the local row table */
+/* float2 per row of the vertically filtered tile Vd: its 127 columns and
+ * what the horizontal items read, a multiple of 2 so that every item's
+ * first column is 16-byte aligned */
+constexpr int kVdPitch = 130;
+__host__ __device__ constexpr int dtma_vd_pitch(int) { return kVdPitch; }
 __host__ __device__ constexpr size_t dtma_main_bytes(int r, int eb)
 {
     return 2 * ((dtma_tile_bytes(r, eb) + 127) / 128 * 128) >
-                   sizeof(float2) * kDY * (size_t)dec_width(r)
+                   sizeof(float2) * kDY * (size_t)dtma_vd_pitch(r)
                ? 2 * ((dtma_tile_bytes(r, eb) + 127) / 128 * 128)
-               : sizeof(float2) * kDY * (size_t)dec_width(r);
+               : sizeof(float2) * kDY * (size_t)dtma_vd_pitch(r);
 }
 __host__ __device__ constexpr size_t dtma_rows_offset(int r, int eb)
 {
@@ -145,6 +150,7 @@ __global__ void __launch_bounds__(kDecThreads)
     constexpr int DW = dec_width(R);
     constexpr int BW = dtma_bw(R, EB);
     constexpr int BH = dtma_bh(R);
+    constexpr int VP = dtma_vd_pitch(R);
     constexpr uint32_t kTileBytes = (uint32_t)dtma_tile_bytes(R, EB);
     constexpr size_t kTileStride = (dtma_tile_bytes(R, EB) + 127) / 128 * 128;
     static_assert(N > 0 && N <= kMaxFixedTaps, "fixed widths only");
@@ -237,23 +243,62 @@ __global__ void __launch_bounds__(kDecThreads)
         const int g = item / DW;
 #pragma unroll
         for (int i = 0; i < kDRV; ++i)
-            Vd[(g * kDRV + i) * DW + cl] = acc[i];
+            Vd[(g * kDRV + i) * VP + cl] = acc[i];
     }
     __syncthreads();
     float2 *dst = a.dst + (size_t)f * a.dst_frame_elems;
-    for (int it = threadIdx.x; it < kDY * DX; it += kDecThreads) {
-        const int yl = it / DX, xl = it % DX;
-        const int yd = y0 + yl, xd = x0 + xl;
-        if (yd >= H2 || xd >= W2)
-            continue;
-        const float2 *in = Vd + yl * DW + 2 * xl;
-        float2 sum;
+    if constexpr (N > 9) {
+        /* wide kernels: one output per item (two would hold 2N+4 registers
+         * of columns and cost occupancy) */
+        for (int it = threadIdx.x; it < kDY * DX; it += kDecThreads) {
+            const int yl = it / DX, xl = it % DX;
+            const int yd = y0 + yl, xd = x0 + xl;
+            if (yd >= H2 || xd >= W2)
+                continue;
+            const float2 *in = Vd + yl * VP + 2 * xl;
+            float2 sum;
 #pragma unroll
-        for (int k = 0; k < N; ++k) {
-            const float2 p = mul2_rn(tp.t2[k], in[k]);
-            sum = (k == 0) ? p : acc2_rn(sum, p, tp.one2);
+            for (int k = 0; k < N; ++k) {
+                const float2 p = mul2_rn(tp.t2[k], in[k]);
+                sum = (k == 0) ? p : acc2_rn(sum, p, tp.one2);
+            }
+            dst[(size_t)yd * W2 + xd] = sum;
         }
-        dst[(size_t)yd * W2 + xd] = sum;
+        return;
+    }
+    /* horizontal pass: two adjacent outputs per item, their N + 2 filtered
+     * columns read as 16-byte pairs of float2; items run along a row */
+    constexpr int kHI = (DX + 1) / 2;       /* two-output items per row */
+    constexpr int kPairs = (N + 3) / 2;     /* 16-byte reads per item   */
+    static_assert(2 * 2 * (kHI - 1) + 2 * kPairs <= kVdPitch,
+                  "Vd reads stay inside a row");
+    for (int it = threadIdx.x; it < kDY * kHI; it += kDecThreads) {
+        const int yl = it / kHI, xl = (it - yl * kHI) * 2;
+        const int yd = y0 + yl;
+        if (yd >= H2)
+            continue;
+        const float4 *row =
+            reinterpret_cast<const float4 *>(Vd + yl * VP + 2 * xl);
+        float2 col[2 * kPairs];
+#pragma unroll
+        for (int u = 0; u < kPairs; ++u) {
+            const float4 v = row[u];
+            col[2 * u] = make_float2(v.x, v.y);
+            col[2 * u + 1] = make_float2(v.z, v.w);
+        }
+#pragma unroll
+        for (int o = 0; o < 2; ++o) {
+            const int xd = x0 + xl + o;
+            if (xl + o >= DX || xd >= W2)
+                break;
+            float2 sum;
+#pragma unroll
+            for (int k = 0; k < N; ++k) {
+                const float2 p = mul2_rn(tp.t2[k], col[2 * o + k]);
+                sum = (k == 0) ? p : acc2_rn(sum, p, tp.one2);
+            }
+            dst[(size_t)yd * W2 + xd] = sum;
+        }
     }
 }
 
