@@ -72,7 +72,7 @@ extern "C" void *fvif_host_alloc(size_t bytes)
         munmap(reinterpret_cast<void *>(a + size), r + align - a);
     void *p = reinterpret_cast<void *>(a);
     madvise(p, size, MADV_HUGEPAGE); /* advice only: ignored if refused */
-    if (cudaHostRegister(p, size, cudaHostRegisterDefault) != cudaSuccess) {
+    if (cudaHostRegister(p, size, cudaHostRegisterPortable) != cudaSuccess) {
         cudaGetLastError();
         munmap(p, size);
         return nullptr;
