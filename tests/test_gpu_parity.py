@@ -346,6 +346,28 @@ def test_host_alloc_buffers(fv):
     assert L.fvif_host_alloc(0) is None
 
 
+def test_alu_probe_counts_and_rate(fv):
+    """fvif_alu_probe: the operation count is 2 ops x 8 chains x iters per
+    thread of 4 CTAs of 256 per SM, the event time is positive, and the
+    rate lies between a quarter of and a little above one rounded operation
+    per lane per clock (152 SMs x 128 lanes x the maximum SM clock)."""
+    torch = torch_mod()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for packed in (False, True):
+        fv.fvif_alu_probe(packed, 1000)
+        ops, ms = fv.fvif_alu_probe(packed, 200_000)
+        assert ops == 2 * 8 * 200_000 * sms * 4 * 256
+        assert ms > 0.0
+        rate = ops / (ms / 1e3)
+        lanes_per_clock = sms * 128 * 2.07e9
+        assert 0.25 * lanes_per_clock < rate < 1.1 * lanes_per_clock, rate
+    L = fv.lib()
+    import ctypes
+    d = ctypes.c_double()
+    assert L.fvif_alu_probe(0, 0, None, ctypes.byref(d),
+                            ctypes.byref(d)) == fv.FVIF_EINVAL
+
+
 def test_zero_frames_and_bad_calls(fv):
     torch = torch_mod()
     with fv.Context(64, 48, 8, 1.0, 2.0) as ctx:
