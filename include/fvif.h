@@ -157,8 +157,8 @@ int fvif_score_host(fvif_ctx *ctx, const void *ref, const void *dist,
                     int n_frames, double *out);
 
 /* Page-locked HOST memory for the inputs of fvif_score_host: bytes rounded
- * up to the transparent-huge-page size (at least 2 MiB), aligned to it,
- * advised for huge pages and registered with the CUDA driver
+ * up to 2 MiB, starting on a transparent-huge-page boundary (at least
+ * 2 MiB), advised for huge pages and registered with the CUDA driver
  * (cudaHostRegister) on behalf of every device.  The copy engine moved
  * such buffers at the host link's full rate where large cudaHostAlloc
  * buffers varied by up to 9x.  The pages have no counterpart: this is a

@@ -55,8 +55,12 @@ extern "C" void *fvif_host_alloc(size_t bytes)
 {
     if (bytes == 0)
         return nullptr;
+    /* the start is aligned to the huge-page size; the length is rounded
+     * only to 2 MiB, so a small request does not pin a whole huge page of
+     * the larger sizes some kernels use */
     const size_t align = huge_page_bytes();
-    const size_t size = (bytes + align - 1) / align * align;
+    const size_t gran = (size_t)2 << 20;
+    const size_t size = (bytes + gran - 1) / gran * gran;
     if (size < bytes || size + align < size)
         return nullptr;
     /* map align bytes more than needed, then keep the aligned part */
