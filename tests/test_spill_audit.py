@@ -3,8 +3,9 @@
 
 The VIF kernels are compiled to fit their register budgets (3 CTAs per SM
 for the fixed-width statistic, 2 for the 35-tap one on 16-bit samples)
-without spilling; a change that makes one spill fails here before any GPU
-run.  The float_ssim window kernels trade a few spilled bytes at k = 3, 5,
+without spilling, except the 35-tap one on 8-bit samples (8 bytes, measured
+faster than its spill-free build); a change that makes another one spill
+fails here before any GPU run.  The float_ssim window kernels trade a few spilled bytes at k = 3, 5,
 6 and 7 for a fourth CTA per SM (measured faster); their budget is 32
 bytes of spill stores."""
 import os
@@ -37,22 +38,29 @@ def report(tmp_path_factory):
 
     with ThreadPoolExecutor(min(8, len(_build.SOURCES))) as ex:
         logs = list(ex.map(run, _build.SOURCES))
+    # ptxas prints, per function, "Function properties for NAME" and then
+    # its stack and spill line; the properties of a non-inlined device
+    # function can follow a kernel's own, so each spill line belongs to the
+    # function named just before it, and only kernels are kept
     kernels = {}
     for log in logs:
-        fn = None
+        entry = props = None
         for line in log.splitlines():
             m = re.search(r"Compiling entry function '(\S+)'", line)
             if m:
-                fn = m.group(1)
-                kernels[fn] = {}
+                entry = m.group(1)
+                kernels[entry] = {}
+            m = re.search(r"Function properties for (\S+)", line)
+            if m:
+                props = m.group(1)
             m = re.search(r"(\d+) bytes spill stores, (\d+) bytes spill "
                           r"loads", line)
-            if m and fn:
-                kernels[fn]["spill_st"] = int(m.group(1))
-                kernels[fn]["spill"] = int(m.group(1)) + int(m.group(2))
+            if m and props in kernels:
+                kernels[props]["spill_st"] = int(m.group(1))
+                kernels[props]["spill"] = int(m.group(1)) + int(m.group(2))
             m = re.search(r"Used (\d+) registers", line)
-            if m and fn:
-                kernels[fn]["regs"] = int(m.group(1))
+            if m and entry:
+                kernels[entry]["regs"] = int(m.group(1))
     return kernels
 
 
@@ -65,10 +73,33 @@ def test_every_kernel_is_reported(report):
     assert all("regs" in v and "spill" in v for v in report.values())
 
 
+# The one VIF kernel allowed to spill, with its budget in bytes (stores plus
+# loads): the 35-tap statistic on 8-bit samples spills 8 bytes at its
+# register share of 3 CTAs per SM; built for 2 CTAs per SM it does not
+# spill, and measured slower (4K 8-bit at kernelscale 2: 70.24 against
+# 69.96 ms per step).
+VIF_SPILL_ALLOWED = {"stats_kernelILi35ELNS_7SrcKindE0E": 16}
+
+
 def test_vif_kernels_do_not_spill(report):
-    bad = {k: v for k, v in report.items()
-           if "fvif" in k and v["spill"] > 0}
+    bad = {}
+    for k, v in report.items():
+        if "fvif" not in k:
+            continue
+        allowed = max([b for pat, b in VIF_SPILL_ALLOWED.items() if pat in k],
+                      default=0)
+        if v["spill"] > allowed:
+            bad[k] = v
     assert not bad, bad
+
+
+def test_audit_sees_the_known_spill(report):
+    """The parser attributes each spill line to the function it names: the
+    known 8-byte spill is seen (a helper's properties printed after a
+    kernel's own must not hide it)."""
+    hits = [v for k, v in report.items()
+            if "stats_kernelILi35ELNS_7SrcKindE0E" in k]
+    assert hits and hits[0]["spill_st"] > 0
 
 
 def test_ssim_kernels_within_spill_budget(report):
