@@ -61,6 +61,23 @@ __host__ __device__ constexpr size_t dtma_tile_bytes(int r, int eb)
  * first column is 16-byte aligned */
 constexpr int kVdPitch = 130;
 __host__ __device__ constexpr int dtma_vd_pitch(int) { return kVdPitch; }
+/* Placement of the filtered columns in a Vd row for the two-output
+ * horizontal items (up to 9 taps): 16-byte pair p of a row is stored at
+ * pair p ^ bit3(p), so the eight pairs a quarter warp reads in one load
+ * (every second pair of a run of sixteen) fall on distinct bank groups;
+ * column c (a float2) moves with its pair.  Wider kernels keep the plain
+ * layout. */
+template <int N>
+__device__ __forceinline__ int dtma_swz_pair(int p)
+{
+    return N <= 9 ? p ^ ((p >> 3) & 1) : p;
+}
+template <int N>
+__device__ __forceinline__ int dtma_swz(int c)
+{
+    return N <= 9 ? c ^ (((c >> 4) & 1) << 1) : c;
+}
+
 __host__ __device__ constexpr size_t dtma_main_bytes(int r, int eb)
 {
     return 2 * ((dtma_tile_bytes(r, eb) + 127) / 128 * 128) >
@@ -243,7 +260,7 @@ __global__ void __launch_bounds__(kDecThreads)
         const int g = item / DW;
 #pragma unroll
         for (int i = 0; i < kDRV; ++i)
-            Vd[(g * kDRV + i) * VP + cl] = acc[i];
+            Vd[(g * kDRV + i) * VP + dtma_swz<N>(cl)] = acc[i];
     }
     __syncthreads();
     float2 *dst = a.dst + (size_t)f * a.dst_frame_elems;
@@ -277,12 +294,11 @@ __global__ void __launch_bounds__(kDecThreads)
         const int yd = y0 + yl;
         if (yd >= H2)
             continue;
-        const float4 *row =
-            reinterpret_cast<const float4 *>(Vd + yl * VP + 2 * xl);
+        const float4 *row = reinterpret_cast<const float4 *>(Vd + yl * VP);
         float2 col[2 * kPairs];
 #pragma unroll
         for (int u = 0; u < kPairs; ++u) {
-            const float4 v = row[u];
+            const float4 v = row[dtma_swz_pair<N>(xl + u)];
             col[2 * u] = make_float2(v.x, v.y);
             col[2 * u + 1] = make_float2(v.z, v.w);
         }
