@@ -19,17 +19,24 @@
  *    exact, so each output is the exact window sum rounded once to fp32.
  * This library reaches the same bits without fp64: the sample sums are
  * integers, and the rounding error of each product is recovered exactly and
- * summed exactly.  The window total is then formed in int64 and rounded once
- * to fp32.
+ * summed exactly.  The window total is then formed exactly (in int64, or at
+ * scales up to 8 as an exact fp32 pair) and rounded once to fp32.
  *
  * Scale 1 is no decimation: the outputs are the converted samples, w x h.
  * These are readings of the page: (a) scale 1 means no decimation; (b)
  * round() rounds the real quotient half away from zero; (c) bit depths 9, 11,
  * 13, 14 and 15 divide by 2^(bitdepth - 8), as 10, 12 and 16 do.
  *
- * Environment: FSSIM_KERNEL=general|windows forces the kernel that scales
- * 2..8 on 16-byte rows use (the default picks per scale and sample size, as
- * measured); every choice gives the same bits.
+ * Environment:
+ *  - FSSIM_KERNEL=general|windows|windows_direct forces the kernel that
+ *    scales 2..8 on 16-byte rows use (the default picks per scale and sample
+ *    size, as measured); windows_direct is the window kernel without staging
+ *    its rows in shared memory (scale 3 stages them by default).  Every
+ *    choice gives the same bits.
+ *  - FSSIM_TEST_STAGE_STALL=1: test hook, read by every fssim_decimate call:
+ *    the staged kernel waits for more bytes than its copies bring, so its
+ *    wait runs out after one second and each block reads its rows from
+ *    global memory instead, with the same bits.  Never set it otherwise.
  */
 #ifndef FSSIM_H
 #define FSSIM_H

@@ -251,9 +251,11 @@ def test_8bit_partials_with_unaligned_outputs(fv):
     (8, 2, 1920, 9), (8, 3, 1600, 10), (8, 5, 3840, 11), (8, 6, 2560, 13),
     (8, 7, 3600, 15), (10, 2, 8192, 5), (10, 3, 3840, 7), (10, 4, 1920, 9),
     (10, 5, 800, 12), (12, 6, 1536, 13), (16, 7, 1792, 15), (16, 8, 3840, 17),
-    (8, 3, 48, 7), (16, 2, 16, 16),
+    (8, 3, 48, 7), (16, 2, 16, 16), (8, 3, 1280, 100), (16, 3, 640, 31),
+    (8, 3, 12336, 5), (10, 3, 6160, 4),
 ])
-@pytest.mark.parametrize("kernel", ["auto", "general", "windows"])
+@pytest.mark.parametrize("kernel", ["auto", "general", "windows",
+                                    "windows_direct"])
 def test_window_kernel_chunk_boundaries(fv, monkeypatch, kernel, bitdepth,
                                         scale, w, h):
     """Rows of a multiple of 16 bytes at scales 2..8 take the window kernel
@@ -262,10 +264,44 @@ def test_window_kernel_chunk_boundaries(fv, monkeypatch, kernel, bitdepth,
     chunks of 16 k bytes, the neighbour's half window by shuffle, lane 0 of
     later warps and the first chunk of a second block column loading the
     previous chunk's last vector, the mirrored first window, a partial last
-    chunk, top-of-range samples."""
+    chunk, top-of-range and all-maximum samples (the largest window sums of
+    the fp32 epilogue).  At scale 3 the window kernel stages the block's
+    rows in shared memory unless windows_direct is forced, or the row needs
+    more than one block column (the 12336- and 6160-sample rows); ragged
+    last row blocks."""
     monkeypatch.setenv("FSSIM_KERNEL", kernel)
     rng = np.random.default_rng(w * 7 + scale)
-    for mode in ("random", "top"):
+    for mode in ("random", "top", "max"):
         ref = rand_frames(rng, 2, h, w, bitdepth, mode)
         dist = rand_frames(rng, 2, h, w, bitdepth, mode)
         check(fv, ref, dist, bitdepth, scale)
+
+
+@pytest.mark.parametrize("bitdepth", [8, 10])
+def test_staged_rows_wait_runs_out_and_falls_back(fv, monkeypatch, bitdepth):
+    """The staged window kernel's mbarrier wait is bounded: with the test
+    hook its phase never completes (16 bytes more expected than the copies
+    bring), every block gives up after one second and reads its rows from
+    global memory instead.  The call takes about a second and the outputs
+    are still the oracle's bits; without the hook the same call is fast."""
+    import time
+    import torch
+    rng = np.random.default_rng(bitdepth)
+    w, h = 1280, 720                       # auto scale 3: 54 blocks
+    ref = rand_frames(rng, 1, h, w, bitdepth)
+    dist = rand_frames(rng, 1, h, w, bitdepth)
+    r, d = to_dev(ref), to_dev(dist)
+    want = oracle.ssim_decimate(ref, dist, bitdepth, 0)
+    times = {}
+    for stall in ("1", "0"):
+        monkeypatch.setenv("FSSIM_TEST_STAGE_STALL", stall)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        ro, do = fv.fssim_decimate(r, d, w, h, bitdepth, 0)
+        torch.cuda.synchronize()
+        times[stall] = time.perf_counter() - t0
+        for a, b in zip((ro, do), want):
+            assert np.array_equal(a.cpu().numpy().view(np.uint32),
+                                  b.view(np.uint32)), stall
+    assert 0.9 < times["1"] < 30.0, times
+    assert times["0"] < 0.5, times

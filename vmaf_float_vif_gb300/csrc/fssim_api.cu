@@ -28,7 +28,18 @@ FixedPath fixed_path_override()
         return FixedPath::kGeneral;
     if (std::strcmp(v, "windows") == 0)
         return FixedPath::kWindows;
+    if (std::strcmp(v, "windows_direct") == 0)
+        return FixedPath::kWindowsDirect;
     return FixedPath::kAuto;
+}
+
+/* FSSIM_TEST_STAGE_STALL=1 in the environment: the staged window kernel
+ * waits for 16 bytes more than its copies bring, so its bounded wait runs
+ * out and every block reads global memory instead (tests of that path). */
+unsigned stage_extra_tx()
+{
+    const char *v = std::getenv("FSSIM_TEST_STAGE_STALL");
+    return v && std::atoi(v) != 0 ? 16u : 0u;
 }
 
 } // namespace fssim
@@ -125,6 +136,8 @@ extern "C" int fssim_decimate(int w, int h, int bitdepth, int scale,
     p.out_scale = exact ? p.tap * inv_q : std::ldexp(1.0f, -(q + E));
     p.packed16 = B == 2 && (long long)k * ((1 << bitdepth) - 1) < 65536;
     p.one2 = make_float2(1.0f, 1.0f);
+    p.inv_q = inv_q;
+    p.stage_extra_tx = stage_extra_tx();
 
     /* Tile: up to kMaxTileCols window columns (whole rows at 4K); shared
      * rows hold the groups of V columns those windows touch. */

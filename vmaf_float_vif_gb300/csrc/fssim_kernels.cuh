@@ -21,15 +21,17 @@
  * with both sums integers: sum(s) <= k^2 * 65535 < 2^31 and
  * |sum(e * 2^E)| <= k^2 * 2^15 <= 2^29 for k <= 128.  The int64 total is
  * rounded once to fp32 (__ll2float_rn), and the power-of-two factor is
- * applied exactly.  For power-of-two k the tap is exact: e = 0 and the output
- * is fl(sum(s)) * t * 2^-q.
+ * applied exactly.  (The window kernel, k <= 7, forms the same rounding in
+ * fp32 alone; see there.)  For power-of-two k the tap is exact: e = 0 and
+ * the output is fl(sum(s)) * t * 2^-q.
  *
  * Three kernels, chosen per sample type and scale (measured at 4K):
  *  - ssim_decimate_u8_partials_kernel: 8-bit samples, k = 4 or 8, 16-byte
  *    rows: window partial sums with dp4a, no shared memory; at the HBM
  *    bound.
  *  - ssim_decimate_windows_kernel: k = 2..8, 16-byte rows: each thread owns
- *    16 (8-bit) or 8 (16-bit) whole windows.
+ *    16 (8-bit) or 8 (16-bit) whole windows; at k = 3 the block's rows are
+ *    staged in shared memory by bulk asynchronous copies.
  *  - ssim_decimate_kernel, the general two-phase kernel, for every other
  *    case (any scale, any alignment).  A block takes R output rows by X
  *    output columns of one plane of one frame.  Phase 1: each thread sums V
@@ -80,6 +82,9 @@ struct DecimateParams {
     float out_scale;          // 2^-(q + E), or tap * 2^-q for exact taps
     int packed16;             // 16-bit samples: column sums fit 16 bits
     float2 one2;              // (1, 1)
+    float inv_q;              // 2^-q
+    unsigned stage_extra_tx;  // bytes the staged kernel waits for in excess
+                              // of its copies (0; tests only)
 };
 
 /* Period-2n symmetric mirror: -1 -> 0, n -> n - 1, repeating with period 2n. */
@@ -572,16 +577,119 @@ ssim_decimate_u8_partials_kernel(const DecimateParams p)
  * first chunk of a block column load the previous chunk's last vector with
  * their own rows, and chunk 0 mirrors its first k/2 columns.  The last
  * window of a row never leaves the row (w even), so the right edge needs no
- * mirror.  No shared memory, no barrier. */
+ * mirror.
+ *
+ * Inexact taps end in fp32 alone: with Sw the window's sample sum (an
+ * integer below 2^23) and Ew its exact error sum, s1 = fl(t * Sw) and its
+ * error fma(Sw, t, -s1) are exact, so is d = error - Ew (both multiples of
+ * 2^-E below 2^24 * 2^-E for k <= 7), and fl(s1 + d) is the one rounding of
+ * t * Sw - Ew, as the int64 form of the header would give it.
+ *
+ * kStaged (k = 3, one block column spanning the row): the block's input rows
+ * come into shared memory by bulk asynchronous copies on one mbarrier, and
+ * the k vectors per row are read from there; a block whose copies did not
+ * arrive within the time limit reads global memory instead.  Otherwise no
+ * shared memory and no barrier. */
 /* CTAs per SM the window kernel's register allocation must allow: 4
  * (64 registers) against 3 at 76-80 registers measured 4-9% faster at
- * k = 3 and 6, though k = 3, 5, 6, 7 then spill a few bytes. */
+ * k = 3 and 6, though some widths then spill a few bytes. */
 #ifndef FSSIM_WIN_MINB
 #define FSSIM_WIN_MINB 4
 #endif
+/* Shared-memory budget of the staged window kernel (k = 3): the block's
+ * input rows and the mbarrier. */
+constexpr size_t kStageMaxBytes = 48 * 1024;
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok)
+                 : "r"(bar), "r"(parity)
+                 : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t a)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(a));
+    return v;
+}
+
+/* The staged window kernel's tile: input row K*(y0 + r) - K/2 + i
+ * (mirrored) of the plane at src goes to shared row r*K + i, r < rn, i < K,
+ * one bulk copy per row issued by the lanes of warp 0, all completing on
+ * one mbarrier placed after the K*R rows.  Every thread waits for the copies
+ * for at most one second; returns true when all of them arrived in time in
+ * every thread of the block (one vote). */
 template <typename T, int K>
-__global__ void __launch_bounds__(kThreads, FSSIM_WIN_MINB)
-ssim_decimate_windows_kernel(const DecimateParams p)
+__device__ __forceinline__ bool stage_rows(const DecimateParams &p,
+                                           const T *src, int y0, int rn,
+                                           uint32_t tile)
+{
+    const uint32_t rowb = (uint32_t)p.w * (uint32_t)sizeof(T);
+    const int nrows = K * rn;
+    const uint32_t bar = tile + (uint32_t)(K * p.R) * rowb;
+    if (threadIdx.x == 0) {
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar)
+                     : "memory");
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        if (threadIdx.x == 0)
+            asm volatile(
+                "mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(
+                    bar),
+                "r"((uint32_t)nrows * rowb + p.stage_extra_tx)
+                : "memory");
+        __syncwarp();
+        for (int j = threadIdx.x; j < nrows; j += 32) {
+            const int r = j / K, i = j - r * K;
+            const T *row = src + (size_t)mirror2n(K * (y0 + r) - K / 2 + i,
+                                                  p.h) * p.w;
+            asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::"
+                         "complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                             tile + (uint32_t)j * rowb),
+                         "l"(reinterpret_cast<uint64_t>(row)), "r"(rowb),
+                         "r"(bar)
+                         : "memory");
+        }
+    }
+    bool arrived = mbar_try_wait(bar, 0);
+    if (!arrived) {
+        const uint64_t t0 = global_ns();
+        while (!(arrived = mbar_try_wait(bar, 0)) &&
+               global_ns() - t0 < 1000000000ull) {
+        }
+    }
+    return !__syncthreads_or(!arrived);
+}
+
+/* The window kernel's work for one block; kTile: the block's input rows
+ * are in shared memory at tile (row r*K + i for output row r of the
+ * block), else they are read from global memory. */
+template <typename T, int K, bool kTile>
+__device__ __forceinline__ void windows_rows(const DecimateParams &p,
+                                             uint32_t tile)
 {
     static_assert(K >= 2 && K <= 8, "window kernel for k = 2..8");
     constexpr bool kExact = (K & (K - 1)) == 0;
@@ -633,16 +741,28 @@ ssim_decimate_windows_kernel(const DecimateParams p)
         float Ep = 0.0f;                  // the mirror of this chunk's start
         if (act) {
             for (int i = 0; i < K; ++i) {
-                const T *rp = chunk + (size_t)mirror2n(yb + i, h) * w;
                 uint4 q[K];
                 uint4 qp = make_uint4(0u, 0u, 0u, 0u);
+                if constexpr (kTile) {
+                    const uint32_t ra =
+                        tile + (uint32_t)((r * K + i) * w + NS * g) *
+                                   (uint32_t)sizeof(T);
 #pragma unroll
-                for (int v = 0; v < K; ++v)
-                    q[v] = v < nvec
-                               ? __ldg(reinterpret_cast<const uint4 *>(rp) + v)
-                               : make_uint4(0u, 0u, 0u, 0u);
-                if (need_prev)
-                    qp = __ldg(reinterpret_cast<const uint4 *>(rp) - 1);
+                    for (int v = 0; v < K; ++v)
+                        q[v] = v < nvec ? lds128(ra + 16u * v)
+                                        : make_uint4(0u, 0u, 0u, 0u);
+                    if (need_prev)
+                        qp = lds128(ra - 16u);
+                } else {
+                    const T *rp = chunk + (size_t)mirror2n(yb + i, h) * w;
+#pragma unroll
+                    for (int v = 0; v < K; ++v)
+                        q[v] = v < nvec ? __ldg(reinterpret_cast<const uint4 *>(
+                                              rp) + v)
+                                        : make_uint4(0u, 0u, 0u, 0u);
+                    if (need_prev)
+                        qp = __ldg(reinterpret_cast<const uint4 *>(rp) - 1);
+                }
 #pragma unroll
                 for (int v = 0; v < K; ++v) {
                     const unsigned wd[4] = {q[v].x, q[v].y, q[v].z, q[v].w};
@@ -728,10 +848,15 @@ ssim_decimate_windows_kernel(const DecimateParams p)
                     o[i] = __fmul_rn(__uint2float_rn(Sw), p.out_scale);
                 } else {
                     const float Ew = i == 0 ? __fadd_rn(E[0], Ep) : E[i];
-                    const long long n =
-                        p.T * (long long)Sw -
-                        (long long)__float2int_rn(__fmul_rn(Ew, p.err_scale));
-                    o[i] = __fmul_rn(__ll2float_rn(n), p.out_scale);
+                    /* the exact window sum t * Sw - Ew, Ew exact in fp32:
+                     * s1 = fl(t * Sw), its error by FMA (exact), then
+                     * d = error - Ew (exact) and one rounding of s1 + d */
+                    const float sf = __fsub_rn(
+                        __uint_as_float(Sw | 0x4b000000u), 8388608.0f);
+                    const float s1 = __fmul_rn(sf, p.tap);
+                    const float d =
+                        __fsub_rn(__fmaf_rn(sf, p.tap, -s1), Ew);
+                    o[i] = __fmul_rn(__fadd_rn(s1, d), p.inv_q);
                 }
             }
             /* a thread's outputs are consecutive: whole chunks go out as
@@ -754,6 +879,40 @@ ssim_decimate_windows_kernel(const DecimateParams p)
                         orow[i] = o[i];
             }
         }
+    }
+}
+
+/* The global-memory form of a staged block whose rows did not arrive in
+ * time; kept out of line so that it costs the staged form no registers. */
+template <typename T, int K>
+__device__ __noinline__ void windows_rows_global(const DecimateParams p)
+{
+    windows_rows<T, K, false>(p, 0u);
+}
+
+template <typename T, int K, bool kStaged>
+__global__ void __launch_bounds__(kThreads, FSSIM_WIN_MINB)
+ssim_decimate_windows_kernel(const DecimateParams p)
+{
+    if constexpr (kStaged) {
+        /* all input rows of the block in shared memory (p.R <= m, one row
+         * of outputs per thread); if they did not arrive within the time
+         * limit, the block reads global memory as the unstaged kernel does,
+         * with the same results */
+        extern __shared__ __align__(16) unsigned char stage_smem[];
+        const uint32_t tile = smem_u32(stage_smem);
+        const int plane = blockIdx.z & 1;
+        const size_t f = blockIdx.z >> 1;
+        const T *src = static_cast<const T *>(plane ? p.src[1] : p.src[0]) +
+                       f * p.in_frame_elems;
+        const int y0 = blockIdx.y * p.R;
+        const int rn = min(p.R, p.sh - y0);
+        if (stage_rows<T, K>(p, src, y0, rn, tile))
+            windows_rows<T, K, true>(p, tile);
+        else
+            windows_rows_global<T, K>(p);
+    } else {
+        windows_rows<T, K, false>(p, 0u);
     }
 }
 
@@ -832,14 +991,23 @@ cudaError_t launch_partials(DecimateParams p, int n_frames,
 /* Launch shape of the window kernel: p.X chunks per block column, p.R output
  * rows per block. */
 template <typename T, int K>
-cudaError_t launch_windows(DecimateParams p, int n_frames,
+cudaError_t launch_windows(DecimateParams p, int n_frames, bool allow_stage,
                            cudaStream_t stream)
 {
     constexpr int WT = 16 / sizeof(T);
     const int G = (p.sw + WT - 1) / WT;
     p.X = G < kThreads ? G : kThreads;
     const int m = kThreads / p.X;
-    p.R = 2 * m < p.sh ? 2 * m : p.sh;
+    const size_t rowb = (size_t)p.w * sizeof(T);
+    /* staged: k = 3, one block column spans the row, one row of outputs
+     * per thread, the block's K*m input rows fit the shared-memory budget
+     * (measured at k = 3 only: 720p and 4K 8-bit, 3-6% faster) */
+    const bool staged = allow_stage && K == 3 && G <= kThreads &&
+                        (size_t)K * m * rowb + 16 <= kStageMaxBytes;
+    p.R = staged ? m : 2 * m;
+    if (p.R > p.sh)
+        p.R = p.sh;
+    const size_t smem = staged ? (size_t)K * p.R * rowb + 16 : 0;
     DecimateParams q = p;
     const size_t in_bytes = p.in_frame_elems * sizeof(T);
     for (int f0 = 0; f0 < n_frames; f0 += kMaxFramesPerLaunch) {
@@ -851,7 +1019,17 @@ cudaError_t launch_windows(DecimateParams p, int n_frames,
             q.dst[s] = p.dst[s] + p.out_frame_elems * (size_t)f0;
         }
         const dim3 grid((G + p.X - 1) / p.X, (p.sh + p.R - 1) / p.R, 2 * nf);
-        ssim_decimate_windows_kernel<T, K><<<grid, kThreads, 0, stream>>>(q);
+        bool launched = false;
+        if constexpr (K == 3) {
+            if (staged) {
+                ssim_decimate_windows_kernel<T, K, true>
+                    <<<grid, kThreads, smem, stream>>>(q);
+                launched = true;
+            }
+        }
+        if (!launched)
+            ssim_decimate_windows_kernel<T, K, false>
+                <<<grid, kThreads, 0, stream>>>(q);
         const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess)
             return e;
@@ -861,8 +1039,9 @@ cudaError_t launch_windows(DecimateParams p, int n_frames,
 
 /* Which kernel takes a fixed scale on the vector path: the window kernel or
  * the general two-phase one (measured choice per sample type and scale;
- * FSSIM_KERNEL=general or =windows in the environment overrides it). */
-enum class FixedPath { kAuto, kGeneral, kWindows };
+ * FSSIM_KERNEL=general, =windows or =windows_direct in the environment
+ * overrides it, the last one the window kernel without staging). */
+enum class FixedPath { kAuto, kGeneral, kWindows, kWindowsDirect };
 FixedPath fixed_path_override();
 
 template <typename T, int K>
@@ -881,9 +1060,11 @@ cudaError_t launch_fixed(const DecimateParams &p, bool vec, int n_frames,
     if (vec) {
         const FixedPath o = fixed_path_override();
         const bool windows = o == FixedPath::kAuto ? prefer_windows<T, K>()
-                                                   : o == FixedPath::kWindows;
+                                                   : o != FixedPath::kGeneral;
         if (windows)
-            return launch_windows<T, K>(p, n_frames, stream);
+            return launch_windows<T, K>(p, n_frames,
+                                        o != FixedPath::kWindowsDirect,
+                                        stream);
         return launch<T, K, kExact, true>(p, n_frames, smem, stream);
     }
     return launch<T, K, kExact, false>(p, n_frames, smem, stream);
