@@ -302,6 +302,23 @@ __global__ void __launch_bounds__(kDecThreads)
             col[2 * u] = make_float2(v.x, v.y);
             col[2 * u + 1] = make_float2(v.z, v.w);
         }
+        /* both outputs inside the row and a 16-byte aligned pair (even
+         * row length, aligned plane): one vector store */
+        if (DX % 2 == 0 && (W2 & 1) == 0 && x0 + xl + 1 < W2 &&
+            (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
+            float2 sum[2];
+#pragma unroll
+            for (int o = 0; o < 2; ++o) {
+#pragma unroll
+                for (int k = 0; k < N; ++k) {
+                    const float2 p = mul2_rn(tp.t2[k], col[2 * o + k]);
+                    sum[o] = (k == 0) ? p : acc2_rn(sum[o], p, tp.one2);
+                }
+            }
+            *reinterpret_cast<float4 *>(dst + (size_t)yd * W2 + x0 + xl) =
+                make_float4(sum[0].x, sum[0].y, sum[1].x, sum[1].y);
+            continue;
+        }
 #pragma unroll
         for (int o = 0; o < 2; ++o) {
             const int xd = x0 + xl + o;
