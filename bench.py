@@ -951,7 +951,8 @@ def main():
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="c5_4k_10b")
     ap.add_argument("--frames", type=int, default=None,
                     help="frames per step (default: the workload's)")
-    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--e2e-steps", type=int, default=None,
+                    help="timed fvif_score_host steps (default: --steps)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-ssim", action="store_true",
@@ -968,6 +969,8 @@ def main():
                          "oracle baseline (\"\" = none; default: every "
                          "other workload)")
     args = ap.parse_args()
+    if args.e2e_steps is None:
+        args.e2e_steps = max(1, args.steps)
     for name in (args.also or "").split(","):
         if name and name not in WORKLOADS:
             ap.error("--also: unknown workload %r (choose from %s)" %
